@@ -1,0 +1,3 @@
+"""fp64 CPU oracle for the attention forward pass (test infrastructure only)."""
+
+from .oracle import attn_fwd, attn_rows, build, default_threads  # noqa: F401

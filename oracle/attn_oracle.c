@@ -1,0 +1,260 @@
+/*
+ * attn_oracle.c -- fp64 CPU oracle for the multi-head scaled dot-product
+ * attention forward pass.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the CPU-baseline leg
+ * of the benchmark load this library. The CUDA path never calls it and shares
+ * no code, header, constant or helper with it.
+ *
+ * What it computes is the plain definition, step by step, for every head
+ * independently and for every query row i (no tiling, no online rescaling):
+ *
+ *   s_j   = scale * sum_t q_it k_jt                 scores of row i
+ *           ("Transformer 详解" §4.1 steps 2-3; "从 RNN 到 Transformer（二）"
+ *            §4.3 steps 2-3 and §4.9: scores = Q Kᵀ / sqrt(d_k))
+ *   J     = keys visible to row i under the mask:
+ *           none         every j                     (encoder self-attention,
+ *                                                     "Transformer 详解" §4.1;
+ *                                                     cross-attention §5.4)
+ *           causal       j <= i                      ("Transformer 详解" §5.3
+ *                                                     Mask_ij = 0 if j<=i else
+ *                                                     -inf; "第2章：完整的
+ *                                                     Transformer 架构" §6)
+ *           key padding  j < len_b, all query rows   ("Transformer 详解" §3.4:
+ *                                                     mask [batch,1,1,seq]
+ *                                                     broadcasts over heads and
+ *                                                     queries, masks keys)
+ *   mu    = max_{j in J} s_j;  Z = sum_{j in J} exp(s_j - mu)
+ *   w_j   = exp(s_j - mu) / Z for j in J, 0 otherwise      (row softmax; the
+ *           shift by mu leaves the value unchanged and keeps exp in range)
+ *   o_i   = sum_j w_j v_j                            ("从 RNN 到 Transformer（二）"
+ *                                                     §4.3 step 5, weighted sum)
+ *   LSE_i = mu + ln Z  (natural log of the masked sum of exp of scaled scores)
+ *
+ * A masked position is excluded from J, which is the -inf fill of the pages'
+ * minimal implementation. With at least one visible key the -1e9 fill of
+ * "Transformer 详解" §3.4 gives the same result in fp64. A row with no
+ * visible key (key length 0) gets o_i = 0 and LSE_i = -inf.
+ *
+ * Key lengths are clamped to [0, m]. Causal masking is defined for any n, m
+ * here as j <= i (the pages only print the square case).
+ *
+ * Layouts: Q [B,H,n,dk], K [B,H,m,dk], V [B,H,m,dv], O [B,H,n,dv], LSE
+ * [B,H,n], all contiguous row-major fp64; key_lengths int32 [B].
+ *
+ * ORACLE_PLANT (compile-time, default 0) plants one known mistake so that the
+ * test suite can show that its pins catch it; the shipped build never sets it.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef ORACLE_PLANT
+#define ORACLE_PLANT 0
+#endif
+
+enum { ORACLE_MASK_NONE = 0, ORACLE_MASK_CAUSAL = 1, ORACLE_MASK_KEY_PADDING = 2 };
+
+/* Is key j visible to query row i? */
+static int visible(int mask_kind, int64_t i, int64_t j, int64_t len)
+{
+    switch (mask_kind) {
+    case ORACLE_MASK_CAUSAL:
+#if ORACLE_PLANT == 2
+        return j < i;              /* planted: diagonal excluded */
+#else
+        return j <= i;
+#endif
+    case ORACLE_MASK_KEY_PADDING:
+#if ORACLE_PLANT == 5
+        return i < len;            /* planted: padding applied to queries */
+#else
+        return j < len;
+#endif
+    default:
+        return 1;
+    }
+}
+
+static int64_t clamp_len(const int32_t* key_lengths, int mask_kind, int64_t b, int64_t m)
+{
+    if (mask_kind != ORACLE_MASK_KEY_PADDING || key_lengths == NULL) return m;
+    int64_t len = key_lengths[b];
+    if (len < 0) len = 0;
+    if (len > m) len = m;
+    return len;
+}
+
+/*
+ * One query row of one head. q [dk], Kh [m,dk], Vh [m,dv] belong to that head.
+ * s and w are caller scratch of m doubles. Writes o [dv], *lse, and, if w_out
+ * is not NULL, the m attention weights of the row.
+ */
+static void attn_row(const double* q, const double* Kh, const double* Vh, int64_t m,
+                     int dk, int dv, int mask_kind, int64_t i, int64_t len, double scale,
+                     double* s, double* o, double* lse, double* w_out)
+{
+    /* 1. scaled scores of every key */
+    for (int64_t j = 0; j < m; ++j) {
+        double dot = 0.0;
+        for (int t = 0; t < dk; ++t) {
+#if ORACLE_PLANT == 3
+            dot += q[t] * Kh[(int64_t)t * dk + (j % dk)];   /* planted: wrong K index */
+#else
+            dot += q[t] * Kh[j * dk + t];
+#endif
+        }
+#if ORACLE_PLANT == 1
+        s[j] = dot;                /* planted: scale dropped */
+#else
+        s[j] = scale * dot;
+#endif
+    }
+    /* 2. maximum over the visible keys */
+    double mu = -INFINITY;
+    int64_t count = 0;
+    for (int64_t j = 0; j < m; ++j) {
+        if (!visible(mask_kind, i, j, len)) continue;
+        if (s[j] > mu) mu = s[j];
+        ++count;
+    }
+    for (int c = 0; c < dv; ++c) o[c] = 0.0;
+    if (count == 0) {
+        *lse = -INFINITY;
+        if (w_out) for (int64_t j = 0; j < m; ++j) w_out[j] = 0.0;
+        return;
+    }
+    /* 3. normaliser and weights */
+    double Z = 0.0;
+    for (int64_t j = 0; j < m; ++j)
+        if (visible(mask_kind, i, j, len)) Z += exp(s[j] - mu);
+    for (int64_t j = 0; j < m; ++j) {
+        double wj = visible(mask_kind, i, j, len) ? exp(s[j] - mu) / Z : 0.0;
+#if ORACLE_PLANT == 6
+        if (j == 0) wj = 0.0;      /* planted: first key dropped from the sum */
+#endif
+        s[j] = wj;
+        if (w_out) w_out[j] = wj;
+    }
+    /* 4. weighted sum of the values, and the logsumexp */
+    for (int64_t j = 0; j < m; ++j) {
+        if (s[j] == 0.0) continue;
+        const double* v = Vh + j * dv;
+        for (int c = 0; c < dv; ++c) o[c] += s[j] * v[c];
+    }
+#if ORACLE_PLANT == 4
+    *lse = log(Z);                 /* planted: max shift not added back */
+#else
+    *lse = mu + log(Z);
+#endif
+}
+
+typedef struct {
+    const double *Q, *K, *V;
+    const int32_t* key_lengths;
+    int64_t B, H, n, m;
+    int dk, dv, mask_kind;
+    double scale;
+    double *O, *LSE, *W;
+    const int64_t* rows;   /* NULL: all rows; else flat indices into [B*H*n] */
+    int64_t nrows;
+    int nthreads, tid;
+} job_t;
+
+static void* worker(void* arg)
+{
+    job_t* jb = (job_t*)arg;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(jb->m > 0 ? jb->m : 1));
+    if (!s) return (void*)1;
+    if (jb->rows == NULL) {
+        /* every (b,h) pair this thread owns, every row of it */
+        for (int64_t bh = jb->tid; bh < jb->B * jb->H; bh += jb->nthreads) {
+            int64_t b = bh / jb->H;
+            int64_t len = clamp_len(jb->key_lengths, jb->mask_kind, b, jb->m);
+            const double* Kh = jb->K + bh * jb->m * jb->dk;
+            const double* Vh = jb->V + bh * jb->m * jb->dv;
+            for (int64_t i = 0; i < jb->n; ++i) {
+                int64_t r = bh * jb->n + i;
+                attn_row(jb->Q + r * jb->dk, Kh, Vh, jb->m, jb->dk, jb->dv, jb->mask_kind, i,
+                         len, jb->scale, s, jb->O + r * jb->dv, jb->LSE + r,
+                         jb->W ? jb->W + r * jb->m : NULL);
+            }
+        }
+    } else {
+        /* sampled rows: output k of O/LSE belongs to flat row rows[k] */
+        for (int64_t k = jb->tid; k < jb->nrows; k += jb->nthreads) {
+            int64_t r = jb->rows[k];
+            int64_t bh = r / jb->n, i = r % jb->n, b = bh / jb->H;
+            int64_t len = clamp_len(jb->key_lengths, jb->mask_kind, b, jb->m);
+            attn_row(jb->Q + r * jb->dk, jb->K + bh * jb->m * jb->dk,
+                     jb->V + bh * jb->m * jb->dv, jb->m, jb->dk, jb->dv, jb->mask_kind, i, len,
+                     jb->scale, s, jb->O + k * jb->dv, jb->LSE + k, NULL);
+        }
+    }
+    free(s);
+    return NULL;
+}
+
+static int run(job_t base)
+{
+    int nt = base.nthreads < 1 ? 1 : base.nthreads;
+    if (nt > 1024) nt = 1024;
+    pthread_t th[1024];
+    job_t jobs[1024];
+    int rc = 0;
+    for (int t = 0; t < nt; ++t) {
+        jobs[t] = base;
+        jobs[t].nthreads = nt;
+        jobs[t].tid = t;
+    }
+    if (nt == 1) return worker(&jobs[0]) == NULL ? 0 : -1;
+    int started = 0;
+    for (int t = 0; t < nt; ++t) {
+        if (pthread_create(&th[t], NULL, worker, &jobs[t]) != 0) { rc = -1; break; }
+        ++started;
+    }
+    for (int t = 0; t < started; ++t) {
+        void* ret = NULL;
+        pthread_join(th[t], &ret);
+        if (ret != NULL) rc = -1;
+    }
+    return rc;
+}
+
+static int bad_args(int64_t B, int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind)
+{
+    return B < 0 || H < 0 || n < 0 || m < 0 || dk < 1 || dv < 1 || mask_kind < 0 ||
+           mask_kind > 2;
+}
+
+/* Full forward: O [B,H,n,dv] and LSE [B,H,n]. W (optional, [B,H,n,m]) gets the
+ * attention weights for small debugging cases. Returns 0 on success. */
+int oracle_attn_fwd(const double* Q, const double* K, const double* V, int64_t B, int64_t H,
+                    int64_t n, int64_t m, int dk, int dv, int mask_kind,
+                    const int32_t* key_lengths, double scale, double* O, double* LSE,
+                    double* W, int nthreads)
+{
+    if (bad_args(B, H, n, m, dk, dv, mask_kind)) return -1;
+    if (mask_kind == ORACLE_MASK_KEY_PADDING && key_lengths == NULL) return -1;
+    job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, O, LSE, W,
+                NULL, 0, nthreads, 0};
+    return run(jb);
+}
+
+/* Selected rows only: rows[k] is a flat index b*H*n + h*n + i; O is [nrows,dv]
+ * and LSE [nrows]. Used to check full-size outputs one row at a time. */
+int oracle_attn_rows(const double* Q, const double* K, const double* V, int64_t B, int64_t H,
+                     int64_t n, int64_t m, int dk, int dv, int mask_kind,
+                     const int32_t* key_lengths, double scale, const int64_t* rows,
+                     int64_t nrows, double* O, double* LSE, int nthreads)
+{
+    if (bad_args(B, H, n, m, dk, dv, mask_kind) || rows == NULL || nrows < 0) return -1;
+    if (mask_kind == ORACLE_MASK_KEY_PADDING && key_lengths == NULL) return -1;
+    for (int64_t k = 0; k < nrows; ++k)
+        if (rows[k] < 0 || rows[k] >= B * H * n) return -1;
+    job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, O, LSE, NULL,
+                rows, nrows, nthreads, 0};
+    return run(jb);
+}

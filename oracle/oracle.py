@@ -1,0 +1,153 @@
+"""Python loader for the fp64 CPU attention oracle (``attn_oracle.c``).
+
+TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU
+baseline leg import this module. It compiles ``attn_oracle.c`` with gcc into
+``oracle/_build/`` and calls it through ctypes. It imports nothing from the
+CUDA package and the CUDA package imports nothing from here.
+
+Inputs may be torch tensors (any float dtype; bf16 widens to fp64 exactly) or
+numpy arrays. Outputs are fp64 numpy arrays.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "attn_oracle.c")
+BUILD_DIR = os.path.join(HERE, "_build")
+
+# The oracle's own mask codes (independent of the CUDA library's enum).
+MASK_CODES = {"none": 0, "causal": 1, "key_padding": 2}
+
+_lock = threading.Lock()
+_libs: dict[int, ctypes.CDLL] = {}
+
+
+def lib_path(plant: int = 0) -> str:
+    name = "libattn_oracle.so" if plant == 0 else f"libattn_oracle_plant{plant}.so"
+    return os.path.join(BUILD_DIR, name)
+
+
+def build(plant: int = 0, force: bool = False) -> str:
+    """Compile the oracle (plain C11, -O2, no fast-math) and return the .so path.
+
+    ``plant`` > 0 builds a copy with one planted mistake (tests only)."""
+    out = lib_path(plant)
+    with _lock:
+        if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(SRC):
+            return out
+        os.makedirs(BUILD_DIR, exist_ok=True)
+        tmp = f"{out}.{os.getpid()}.tmp"
+        cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread",
+               f"-DORACLE_PLANT={int(plant)}", SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def _load(plant: int = 0) -> ctypes.CDLL:
+    if plant in _libs:
+        return _libs[plant]
+    lib = ctypes.CDLL(build(plant))
+    dp = ctypes.POINTER(ctypes.c_double)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    ci = ctypes.c_int
+    lib.oracle_attn_fwd.argtypes = [dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p,
+                                    ctypes.c_double, dp, dp, dp, ci]
+    lib.oracle_attn_fwd.restype = ci
+    lib.oracle_attn_rows.argtypes = [dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p,
+                                     ctypes.c_double, i64p, i64, dp, dp, ci]
+    lib.oracle_attn_rows.restype = ci
+    _libs[plant] = lib
+    return lib
+
+
+def _f64(x) -> np.ndarray:
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _lens(key_lengths, B):
+    if key_lengths is None:
+        return None
+    arr = np.ascontiguousarray(np.asarray(
+        key_lengths.cpu().numpy() if hasattr(key_lengths, "cpu") else key_lengths,
+        dtype=np.int32).reshape(B))
+    return arr
+
+
+def _ptr(a, ctype):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def default_threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover
+        return max(1, os.cpu_count() or 1)
+
+
+def _shapes(Q, K, V):
+    if Q.ndim != 4 or K.ndim != 4 or V.ndim != 4:
+        raise ValueError("Q, K, V must be [B, H, L, d]")
+    B, H, n, dk = Q.shape
+    m = K.shape[2]
+    dv = V.shape[3]
+    if K.shape != (B, H, m, dk) or V.shape[:3] != (B, H, m):
+        raise ValueError("inconsistent Q/K/V shapes")
+    return B, H, n, m, dk, dv
+
+
+def attn_fwd(Q, K, V, mask="none", key_lengths=None, scale=None, *, threads=None,
+             weights=False, plant=0):
+    """Oracle forward. Returns (O [B,H,n,dv], LSE [B,H,n]) or, with weights=True,
+    (O, LSE, W [B,H,n,m]). ``scale`` defaults to 1/sqrt(d_k)."""
+    Qd, Kd, Vd = _f64(Q), _f64(K), _f64(V)
+    B, H, n, m, dk, dv = _shapes(Qd, Kd, Vd)
+    sc = 1.0 / np.sqrt(dk) if scale is None else float(scale)
+    lens = _lens(key_lengths, B)
+    O = np.zeros((B, H, n, dv))
+    L = np.zeros((B, H, n))
+    W = np.zeros((B, H, n, m)) if weights else None
+    rc = _load(plant).oracle_attn_fwd(
+        _ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
+        B, H, n, m, dk, dv, MASK_CODES[mask], _ptr(lens, ctypes.c_int32), sc,
+        _ptr(O, ctypes.c_double), _ptr(L, ctypes.c_double), _ptr(W, ctypes.c_double),
+        threads or min(default_threads(), 16))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_fwd failed ({rc})")
+    return (O, L, W) if weights else (O, L)
+
+
+def attn_rows(Q, K, V, rows, mask="none", key_lengths=None, scale=None, *, threads=None,
+              plant=0):
+    """Oracle outputs for selected flat rows (b*H*n + h*n + i): (O [k,dv], LSE [k])."""
+    Qd, Kd, Vd = _f64(Q), _f64(K), _f64(V)
+    B, H, n, m, dk, dv = _shapes(Qd, Kd, Vd)
+    sc = 1.0 / np.sqrt(dk) if scale is None else float(scale)
+    lens = _lens(key_lengths, B)
+    r = np.ascontiguousarray(np.asarray(
+        rows.cpu().numpy() if hasattr(rows, "cpu") else rows, dtype=np.int64).reshape(-1))
+    O = np.zeros((r.size, dv))
+    L = np.zeros((r.size,))
+    rc = _load(plant).oracle_attn_rows(
+        _ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
+        B, H, n, m, dk, dv, MASK_CODES[mask], _ptr(lens, ctypes.c_int32), sc,
+        _ptr(r, ctypes.c_int64), r.size, _ptr(O, ctypes.c_double), _ptr(L, ctypes.c_double),
+        threads or min(default_threads(), 16))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_rows failed ({rc})")
+    return O, L
