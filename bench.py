@@ -1,0 +1,371 @@
+"""Benchmark of the sm_103a attention forward (one JSON line on stdout).
+
+A step is one attention forward pass (one launch of the fused kernel) over one
+batch of the base-encoder workload: B=32, H=8, n=m=512, d_k=d_v=64, bf16,
+heads from bias-free Xavier projections of X ~ N(0,1), key padding with valid
+lengths uniform in [256, 512]. Inputs are synthetic and seeded.
+
+Device timing: the inputs and outputs rotate over enough copies that one pass
+over all of them (> 2x the 129 MB L2) never re-reads a warm copy; the launches
+are captured in a CUDA graph and replayed back to back between CUDA events on
+the launching stream. End-to-end timing goes through the same C entry point
+with pinned host buffers: host->device copy of Q, K, V and the key lengths,
+the forward pass, device->host copy of O and LSE, every step.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores (the only other implementation there is).
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the forward pass has no exchange step); value = all ranks' FLOPs / the slowest
+rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from transformer_scaled_dot_03_gb300 import inputs  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (bf16) at 1 GB300 and % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "base_encoder_keypad"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_workload(name):
+    w = inputs.WORKLOADS[name]
+    x = inputs.workload_inputs(w)
+    return w, x
+
+
+def run_ours(args):
+    import torch.distributed as dist
+    from transformer_scaled_dot_03_gb300 import attn, build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or not os.path.exists(attn.LIB_PATH):
+        build.build()
+    if world > 1:
+        dist.barrier()
+    attn.load()
+
+    w, x = make_workload(args.workload)
+    flops = w.flops()
+    eff_flops = flops
+    if w.mask == inputs.MASK_KEY_PADDING:
+        eff_flops = 4.0 * w.H * w.d_k * w.n * float(x.key_lengths.clamp(0, w.m).sum())
+    in_bytes = x.Q.numel() * 2 + x.K.numel() * 2 + x.V.numel() * 2
+    out_bytes = w.B * w.H * w.n * (w.d_v * 2 + 4)
+    copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_bytes)))
+    stream = torch.cuda.Stream(device=dev)
+    lens_d = x.key_lengths.to(dev) if x.key_lengths is not None else None
+    sets = []
+    with torch.cuda.stream(stream):
+        for _ in range(copies):
+            sets.append((x.Q.to(dev), x.K.to(dev), x.V.to(dev),
+                         torch.empty(w.B, w.H, w.n, w.d_v, dtype=torch.bfloat16, device=dev),
+                         torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)))
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        Q, K, V, O, L = sets[i % copies]
+        attn.attn_fwd(Q, K, V, w.mask, lens_d, x.scale, O=O, LSE=L, stream=stream)
+
+    # warm-up (also creates the status word before any graph capture)
+    for i in range(args.warmup):
+        step(i)
+    rc, detail = attn.device_status(stream)
+    if rc != attn.ATTN_OK:
+        raise RuntimeError(f"device status {rc} ({detail}) after warm-up")
+
+    # capture one graph of G launches over the rotating copies
+    G = copies * max(1, 64 // copies)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(G):
+                step(i)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(1, math.ceil(args.steps / G))
+    K_steps = reps * G
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter()
+        ev0.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+        if world > 1:
+            dist.barrier()
+    dev_ms = ev0.elapsed_time(ev1)
+    rc, detail = attn.device_status(stream)
+    if rc != attn.ATTN_OK:
+        raise RuntimeError(f"device status {rc} ({detail}) after the timed region")
+
+    # end to end through the C entry point with pinned host buffers
+    hQ, hK, hV = x.Q.pin_memory(), x.K.pin_memory(), x.V.pin_memory()
+    hlens = x.key_lengths.pin_memory() if x.key_lengths is not None else None
+    hO = torch.empty(w.B, w.H, w.n, w.d_v, dtype=torch.bfloat16).pin_memory()
+    hL = torch.empty(w.B, w.H, w.n, dtype=torch.float32).pin_memory()
+    dQ, dK, dV, dO, dL = sets[0]
+    dlens = torch.empty_like(lens_d) if lens_d is not None else None
+    e2e_steps = max(3, min(args.e2e_steps, K_steps))
+
+    def e2e_step():
+        dQ.copy_(hQ, non_blocking=True)
+        dK.copy_(hK, non_blocking=True)
+        dV.copy_(hV, non_blocking=True)
+        if dlens is not None:
+            dlens.copy_(hlens, non_blocking=True)
+        attn.attn_fwd(dQ, dK, dV, w.mask, dlens, x.scale, O=dO, LSE=dL, stream=stream)
+        hO.copy_(dO, non_blocking=True)
+        hL.copy_(dL, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = in_bytes + (hlens.numel() * 4 if hlens is not None else 0)
+    d2h = hO.numel() * 2 + hL.numel() * 4
+
+    ms = dev_ms / K_steps
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    value = world * flops / (ms * 1e-3) / 1e12
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    peak, peak_sus, hbm, src = peaks()
+    kernel_tflops = flops / (ms * 1e-3) / 1e12
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(w, x, args.cpu_seconds)
+        clocks = clk.summary()
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; bias-free Xavier projections of X~N(0,1))",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "m": w.m,
+                       "d_k": w.d_k, "d_v": w.d_v, "mask": w.mask,
+                       "key_lengths": [w.len_lo, w.len_hi] if w.mask == "key_padding" else None,
+                       "global_batch": w.B * world, "parallelism": f"replicas{world}",
+                       "l2": f"rotating {copies} input/output sets "
+                             f"({copies * (in_bytes + out_bytes) / 2**20:.0f} MiB > 2x L2)",
+                       "timing": f"CUDA graph of {G} launches x {reps} replays between events"},
+            "pct_of_peak": round(100.0 * value / world / peak, 2),
+            "effective_tflops": round(world * eff_flops / (ms * 1e-3) / 1e12, 2),
+            "roofline": {"bound": "tensor", "achieved": round(kernel_tflops, 2),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
+                         "traffic": args.traffic, "peak_source": f"{src} bf16 burst",
+                         "hbm_gbs_achieved": round((in_bytes + out_bytes) / (ms * 1e-3) / 1e9, 1),
+                         "hbm_frac": round((in_bytes + out_bytes) / (ms * 1e-3) / 1e9 / hbm, 4)},
+            "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": K_steps,
+            "clocks": clocks,
+            "wall_s_timed": round(t_wall, 3),
+        }
+        if cpu is not None:
+            result["cpu_baseline"] = cpu
+    if world > 1:
+        dist.destroy_process_group()
+    return result
+
+
+def cpu_baseline(w, x, seconds):
+    """The fp64 oracle as it stands, on all host cores, over a seeded sample of
+    query rows of the same workload; scaled to TFLOP/s of the nominal FLOP model."""
+    from oracle import oracle
+
+    threads = oracle.default_threads()
+    total_rows = w.B * w.H * w.n
+    per_row = 4.0 * w.m * w.d_k * (0.5 if w.mask == "causal" else 1.0)
+    # calibrate on a small sample, then size the sample to about `seconds`
+    probe = inputs.sample_rows(w.B, w.H, w.n, min(total_rows, 64 * threads), seed=11)
+    t0 = time.perf_counter()
+    oracle.attn_rows(x.Q, x.K, x.V, probe, w.mask, x.key_lengths, x.scale, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    count = int(min(total_rows, max(probe.numel(), probe.numel() * seconds / dt)))
+    rows = inputs.sample_rows(w.B, w.H, w.n, count, seed=12)
+    t0 = time.perf_counter()
+    oracle.attn_rows(x.Q, x.K, x.V, rows, w.mask, x.key_lengths, x.scale, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": round(per_row * rows.numel() / dt / 1e12, 6), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"{rows.numel()} of {total_rows} query rows of {w.name} (seeded), fp64"}
+
+
+def run_reference(args):
+    """The oracle as it stands on the host cores: each step is a bounded seeded sample
+    of query rows of the same workload, sized so that the whole run takes about
+    --cpu-seconds; value = nominal FLOPs of the sampled rows / time."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    w, x = make_workload(args.workload)
+    from oracle import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    total_rows = w.B * w.H * w.n
+    per_row = 4.0 * w.m * w.d_k * (0.5 if w.mask == "causal" else 1.0)
+    probe = inputs.sample_rows(w.B, w.H, w.n, min(total_rows, 16 * threads), seed=21)
+    t0 = time.perf_counter()
+    oracle.attn_rows(x.Q, x.K, x.V, probe, w.mask, x.key_lengths, x.scale, threads=threads)
+    rate = probe.numel() / max(time.perf_counter() - t0, 1e-6)
+    per_step = max(threads, int(rate * args.cpu_seconds / (args.steps + args.warmup)))
+    per_step = min(per_step, total_rows)
+    secs, nrows = [], 0
+    for i in range(args.warmup + args.steps):
+        rows = inputs.sample_rows(w.B, w.H, w.n, per_step, seed=1000 + i)
+        t0 = time.perf_counter()
+        oracle.attn_rows(x.Q, x.K, x.V, rows, w.mask, x.key_lengths, x.scale, threads=threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            secs.append(dt)
+            nrows = rows.numel()
+    total = sum(secs)
+    v = per_row * nrows * len(secs) / total / 1e12
+    ms = w.flops() / (v * 1e12) * 1e3
+    sample = (f"{nrows} of {total_rows} query rows of {w.name} per step (seeded), fp64; "
+              f"ms_per_step extrapolated to the whole workload")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "m": w.m, "d_k": w.d_k,
+                       "d_v": w.d_v, "mask": w.mask, "parallelism": "host cores"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(total, 2)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=65536)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,116 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) multi-head scaled dot-product
+ * attention forward pass.
+ *
+ * Operation ("Transformer 详解" §4.1-§4.2 and §5.3-§5.4; "从 RNN 到 Transformer
+ * （二）" §4.9; "第2章：完整的 Transformer 架构" §2.2, §6, §7): for every batch
+ * entry b, head h and query row i, independently per head,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j( scale * q_i . k_j + M_bij ) v_j
+ *     LSE[b,h,i] = ln sum_{j : M_bij = 0} exp( scale * q_i . k_j )
+ *
+ * where M_bij is 0 for a visible key and -inf for a masked one:
+ *     ATTN_MASK_NONE         every key is visible (encoder self-attention,
+ *                            cross-attention without padding);
+ *     ATTN_MASK_CAUSAL       key j is visible to query i iff j <= i (decoder
+ *                            self-attention, "Transformer 详解" §5.3);
+ *     ATTN_MASK_KEY_PADDING  key j is visible iff j < key_lengths[b], for all
+ *                            query rows (the [batch,1,1,seq] pad mask of
+ *                            "Transformer 详解" §3.4 for tail-padded batches).
+ * The n x m score matrix is never written to memory. LSE is the per-row
+ * natural-log normaliser (not printed on the pages; a standard by-product
+ * needed to merge or differentiate attention).
+ *
+ * Conventions common to every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller. The library neither frees nor retains them.
+ *   - Layouts are contiguous row-major: Q [B,H,n,d_k], K [B,H,m,d_k],
+ *     V [B,H,m,d_v], O [B,H,n,d_v] in bf16 (IEEE bfloat16, 2 bytes); LSE
+ *     [B,H,n] fp32; key_lengths int32 [B].
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronise the host. The return value is the
+ *     enqueue status. Faults inside a kernel surface later from the CUDA
+ *     runtime; a device-side watchdog expiry is reported by
+ *     attn_get_device_status().
+ *   - Memory: the library allocates one 4-byte device status word per device
+ *     on the first call on that device and nothing else.
+ *   - Thread safety: concurrent calls on distinct streams are safe.
+ */
+#ifndef ATTN_SM103A_H
+#define ATTN_SM103A_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_MASK_NONE = 0,
+    ATTN_MASK_CAUSAL = 1,
+    ATTN_MASK_KEY_PADDING = 2
+} attn_mask_kind_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad mask kind,
+                                  causal with n != m, KEY_PADDING without lengths */
+    ATTN_ERR_UNSUPPORTED = -2, /* head dims other than d_k = d_v in {64, 128}, or
+                                  sizes beyond the kernel's index range */
+    ATTN_ERR_MISALIGNED = -3,  /* Q, K, V or O not 16-byte aligned; LSE or
+                                  key_lengths not 4-byte aligned */
+    ATTN_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (message in
+                                  attn_last_error()) */
+    ATTN_ERR_TIMEOUT = -5      /* a device-side bounded wait expired (watchdog) */
+} attn_status_t;
+
+/*
+ * Attention forward. See the file comment for the operation and layouts.
+ *   B, H, n, m   batch, heads, query rows, key/value rows. B, H or n equal to 0
+ *                is a no-op; m = 0 writes O = 0 and LSE = -inf.
+ *   d_k, d_v     head dims; supported: d_k == d_v in {64, 128}.
+ *   mask_kind    attn_mask_kind_t. CAUSAL requires n == m (the pages define the
+ *                square mask only).
+ *   key_lengths  device int32 [B]; required for KEY_PADDING, ignored otherwise.
+ *                Values are read on the device and clamped to [0, m]; a length
+ *                of 0 gives O = 0 and LSE = -inf for every row of that entry.
+ *   scale        multiplies q.k; a value <= 0, NaN or inf selects 1/sqrt(d_k)
+ *                ("从 RNN 到 Transformer（二）" §4.4).
+ *   O            bf16 output [B,H,n,d_v] (round to nearest even).
+ *   LSE          fp32 output [B,H,n], or NULL to skip it.
+ *   stream       cudaStream_t to enqueue on.
+ * Returns ATTN_OK or a negative attn_status_t; on error nothing is enqueued.
+ */
+int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+             int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O,
+             float* LSE, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns ATTN_ERR_TIMEOUT if any kernel since the last call gave up on a
+ * bounded wait (its outputs are then undefined), ATTN_ERR_CUDA if the
+ * synchronisation failed, else ATTN_OK. If `detail` is not NULL it receives the
+ * raw status bits (which wait gave up).
+ */
+int attn_get_device_status(void* stream, uint32_t* detail);
+
+/*
+ * Watchdog settings for subsequent calls from any thread: `limit_ns` is the
+ * wall-clock limit of one device-side wait (0 restores the default, 2 s).
+ * `debug_flags` bit 0 makes every softmax warp wait on a barrier that nothing
+ * completes, with a 20 ms limit, so that tests can exercise the timeout path
+ * without a fault. Not meant to be changed while other threads launch.
+ */
+void attn_set_watchdog(uint64_t limit_ns, uint32_t debug_flags);
+
+/* Human-readable name of a status code. */
+const char* attn_status_string(int status);
+
+/* Message of the last ATTN_ERR_CUDA on the calling thread ("" if none). */
+const char* attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SM103A_H */

@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads,
+exports every function include/attn.h declares, and rejects bad arguments with
+the documented status codes before touching any device memory."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from transformer_scaled_dot_03_gb300 import attn, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return attn.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(attn_[a-z_0-9]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_expected_api():
+    assert declared_functions() == sorted(attn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    nm = os.popen(f"nm -D --defined-only {attn.LIB_PATH}").read()
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}\b", nm), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "ATTN_OK"), (-1, "ATTN_ERR_INVALID_ARG"), (-2, "ATTN_ERR_UNSUPPORTED"),
+                       (-3, "ATTN_ERR_MISALIGNED"), (-4, "ATTN_ERR_CUDA"), (-5, "ATTN_ERR_TIMEOUT")]:
+        assert attn.status_string(code) == name
+
+
+P = ctypes.c_void_p(0x10000)      # aligned fake addresses: never dereferenced (rejected first)
+P2 = ctypes.c_void_p(0x20000)
+
+
+def call(Q=P, K=P, V=P, B=1, H=1, n=4, m=4, dk=64, dv=64, mask=0, lens=None, O=P2, LSE=None):
+    return attn.attn_fwd_raw(Q, K, V, B, H, n, m, dk, dv, mask, lens, -1.0, O, LSE, 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(n=-3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(m=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=1, n=4, m=5), attn.ATTN_ERR_INVALID_ARG),          # causal needs n == m
+    (dict(mask=2, lens=None), attn.ATTN_ERR_INVALID_ARG),         # key padding needs lengths
+    (dict(dk=32, dv=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dk=64, dv=128), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dk=96, dv=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(Q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(O=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Q=ctypes.c_void_p(0x10008)), attn.ATTN_ERR_MISALIGNED),
+    (dict(V=ctypes.c_void_p(0x10002)), attn.ATTN_ERR_MISALIGNED),
+    (dict(O=ctypes.c_void_p(0x20004)), attn.ATTN_ERR_MISALIGNED),
+    (dict(LSE=ctypes.c_void_p(0x30002)), attn.ATTN_ERR_MISALIGNED),
+    (dict(mask=2, lens=ctypes.c_void_p(0x40001)), attn.ATTN_ERR_MISALIGNED),
+])
+def test_rejects_bad_arguments(lib, kw, code):
+    assert call(**kw) == code
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(n=0), dict(B=0, Q=None, O=None)])
+def test_empty_problem_is_a_noop(lib, kw):
+    # nothing to compute: returns OK without touching the device
+    assert call(**kw) == attn.ATTN_OK
+
+
+def test_binding_fails_loudly_without_gpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        attn.attn_fwd(q, q, q)
+
+
+def test_flop_model():
+    assert attn.flops(32, 8, 512, 512, 64, "key_padding") == 4.0 * 32 * 8 * 512 * 512 * 64
+    assert attn.flops(16, 16, 1024, 1024, 64, "causal") == 2.0 * 16 * 16 * 1024 * 1024 * 64

@@ -1,0 +1,48 @@
+"""Device-side watchdog: every wait in the kernel is bounded. A debug flag makes
+the softmax warps wait on a barrier that nothing completes; the kernel must give
+up after its short limit, report ATTN_ERR_TIMEOUT through the status word,
+release its tensor memory and leave the context usable (no trap, no fault)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from transformer_scaled_dot_03_gb300 import attn, build, inputs
+
+pytestmark = pytest.mark.gpu
+
+FORCED_BIT = 8   # status bit of the forced wait
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return attn.load()
+
+
+def _run(x):
+    lens = x.key_lengths.cuda() if x.key_lengths is not None else None
+    return attn.attn_fwd(x.Q.cuda(), x.K.cuda(), x.V.cuda(), x.mask, lens, x.scale)
+
+
+@pytest.mark.parametrize("mask,d", [("none", 64), ("causal", 128), ("key_padding", 64)])
+def test_forced_timeout_reports_and_recovers(mask, d):
+    x = inputs.make_inputs(1, 2, 300, 300, d, d, mask, seed=5000, len_lo=200, len_hi=300)
+    assert attn.device_status() == (attn.ATTN_OK, 0)
+    attn.set_watchdog(0, 1)
+    try:
+        _run(x)
+        rc, detail = attn.device_status()
+    finally:
+        attn.set_watchdog(0, 0)
+    assert rc == attn.ATTN_ERR_TIMEOUT
+    assert detail & FORCED_BIT
+    # the status word was cleared, and a normal call afterwards is correct
+    O, L = _run(x)
+    assert attn.device_status() == (attn.ATTN_OK, 0)
+    Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale)
+    assert np.abs(O.float().cpu().numpy() - Or).max() <= 1e-2
+    assert np.abs(L.cpu().numpy() - Lr).max() <= 1e-3

@@ -1,0 +1,151 @@
+"""Python binding of the C-ABI attention library (``libattn_sm103a.so``).
+
+Argument marshalling only: tensors are checked for dtype, shape, device and
+contiguity, and their device pointers plus PyTorch's current CUDA stream are
+passed to the C entry points declared in ``include/attn.h``. Every step of the
+attention forward pass runs in the library's kernels. There is no fallback:
+if the library is missing or no GPU is present, the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import inputs as _inputs
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn_sm103a.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_MISALIGNED = -3
+ATTN_ERR_CUDA = -4
+ATTN_ERR_TIMEOUT = -5
+
+MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PADDING: 2}
+
+# Every symbol include/attn.h declares.
+EXPORTS = ("attn_fwd", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
+           "attn_last_error")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status}) {detail}".rstrip())
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library (built by ``transformer_scaled_dot_03_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA attention library not built: {path} "
+                               "(run transformer_scaled_dot_03_gb300.build.build())")
+        lib = ctypes.CDLL(path)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp]
+        lib.attn_fwd.restype = i32
+        lib.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.attn_get_device_status.restype = i32
+        lib.attn_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
+        lib.attn_set_watchdog.restype = None
+        lib.attn_status_string.argtypes = [i32]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_last_error.argtypes = []
+        lib.attn_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    return load().attn_last_error().decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def attn_fwd_raw(Q_ptr, K_ptr, V_ptr, B, H, n, m, d_k, d_v, mask_kind, key_lengths_ptr, scale,
+                 O_ptr, LSE_ptr, stream_handle) -> int:
+    """The C entry point with plain integers/pointers; returns the status code."""
+    return load().attn_fwd(Q_ptr, K_ptr, V_ptr, int(B), int(H), int(n), int(m), int(d_k), int(d_v),
+                           int(mask_kind), key_lengths_ptr, ctypes.c_float(scale), O_ptr, LSE_ptr,
+                           ctypes.c_void_p(stream_handle))
+
+
+def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "none",
+             key_lengths: torch.Tensor | None = None, scale: float | None = None,
+             O: torch.Tensor | None = None, LSE: torch.Tensor | None = None,
+             want_lse: bool = True, stream=None):
+    """Attention forward on the GPU. Q [B,H,n,d], K [B,H,m,d], V [B,H,m,d] bf16 CUDA
+    tensors (contiguous); ``key_lengths`` int32 CUDA [B] for ``mask="key_padding"``.
+    Returns (O [B,H,n,d] bf16, LSE [B,H,n] fp32 or None). Asynchronous on ``stream``
+    (default: PyTorch's current stream)."""
+    if mask not in MASK_CODES:
+        raise ValueError(f"unknown mask {mask!r}")
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    B, H, n, d_k = Q.shape
+    m = K.shape[2]
+    d_v = V.shape[3]
+    if tuple(K.shape) != (B, H, m, d_k) or tuple(V.shape[:3]) != (B, H, m):
+        raise ValueError("inconsistent Q/K/V shapes")
+    if mask == "key_padding":
+        if key_lengths is None or key_lengths.dtype != torch.int32 or not key_lengths.is_cuda \
+                or key_lengths.numel() != B or not key_lengths.is_contiguous():
+            raise ValueError("key_padding needs key_lengths: contiguous int32 CUDA [B]")
+    if O is None:
+        O = torch.empty((B, H, n, d_v), dtype=torch.bfloat16, device=Q.device)
+    if LSE is None and want_lse:
+        LSE = torch.empty((B, H, n), dtype=torch.float32, device=Q.device)
+    sc = -1.0 if scale is None else float(scale)
+    rc = attn_fwd_raw(_ptr(Q), _ptr(K), _ptr(V), B, H, n, m, d_k, d_v, MASK_CODES[mask],
+                      _ptr(key_lengths) if mask == "key_padding" else None, sc, _ptr(O), _ptr(LSE),
+                      _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd", last_error() if rc == ATTN_ERR_CUDA else "")
+    return O, LSE
+
+
+def device_status(stream=None) -> tuple[int, int]:
+    """Synchronise the stream; return (status, detail bits) of the device status word."""
+    detail = ctypes.c_uint32(0)
+    rc = load().attn_get_device_status(ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(detail))
+    return rc, int(detail.value)
+
+
+def set_watchdog(limit_ns: int = 0, debug_flags: int = 0) -> None:
+    load().attn_set_watchdog(ctypes.c_uint64(limit_ns), ctypes.c_uint32(debug_flags))
+
+
+def flops(B, H, n, m, d_k, mask) -> float:
+    """Nominal forward FLOPs: 4*B*H*n*m*d_k, halved for causal."""
+    f = 4.0 * B * H * n * m * d_k
+    return f / 2 if mask == "causal" else f
+
+
+def default_scale(d_k: int) -> float:
+    return 1.0 / math.sqrt(d_k)

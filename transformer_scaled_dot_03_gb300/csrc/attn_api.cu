@@ -1,0 +1,223 @@
+// attn_api.cu -- C ABI of the sm_103a attention forward (declared in
+// include/attn.h): argument validation, TMA tensor maps, the per-device
+// status word and the kernel launch.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+
+namespace {
+
+constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;   // 2 s per device-side wait
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+uint32_t* g_status[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+uint64_t g_watchdog_ns = kDefaultWatchdogNs;
+uint32_t g_debug_flags = 0;
+thread_local char g_last_error[256] = "";
+
+int fail_cuda(const char* what, cudaError_t e)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, cudaGetErrorString(e));
+    return ATTN_ERR_CUDA;
+}
+
+int fail_msg(const char* what)
+{
+    snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+    return ATTN_ERR_CUDA;
+}
+
+// The device status word of the current device, created on first use.
+int status_word(uint32_t** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return fail_msg("device index out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_status[dev] == nullptr) {
+        uint32_t* p = nullptr;
+        e = cudaMalloc(&p, sizeof(uint32_t));
+        if (e != cudaSuccess) return fail_cuda("cudaMalloc(status word)", e);
+        e = cudaMemset(p, 0, sizeof(uint32_t));
+        if (e != cudaSuccess) return fail_cuda("cudaMemset(status word)", e);
+        e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) return fail_cuda("cudaDeviceSynchronize", e);
+        g_status[dev] = p;
+    }
+    *out = g_status[dev];
+    return ATTN_OK;
+}
+
+int encoder(PFN_cuTensorMapEncodeTiled_v12000* out)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess) return fail_cuda("cudaGetDriverEntryPointByVersion", e);
+        if (fn == nullptr || q != cudaDriverEntryPointSuccess)
+            return fail_msg("cuTensorMapEncodeTiled not available");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = g_encode;
+    return ATTN_OK;
+}
+
+// 3-D bf16 map over [bh][rows][d] with a {64, box_rows, 1} box and 128-byte swizzle.
+int make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* base, int64_t bh,
+             int64_t rows, int64_t d, uint32_t box_rows)
+{
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(bh)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(rows * d * 2)};
+    cuuint32_t box[3] = {64u, box_rows, 1u};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                     strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (%d)",
+                 static_cast<int>(r));
+        return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}
+
+__global__ void fill_no_keys_kernel(uint16_t* O, int64_t o_elems, float* LSE, int64_t rows)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    for (int64_t i = i0; i < o_elems; i += stride) O[i] = 0;
+    if (LSE != nullptr)
+        for (int64_t i = i0; i < rows; i += stride) LSE[i] = -INFINITY;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+             int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
+             void* stream)
+{
+    if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind == ATTN_MASK_CAUSAL && n != m) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind == ATTN_MASK_KEY_PADDING && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!(d_k == d_v && (d_k == 64 || d_k == 128))) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || n == 0) return ATTN_OK;   // nothing to compute
+    if (O == nullptr || (m > 0 && (Q == nullptr || K == nullptr || V == nullptr)))
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(O, 16) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16))
+        return ATTN_ERR_MISALIGNED;
+    if ((LSE != nullptr && !aligned(LSE, 4)) || (key_lengths != nullptr && !aligned(key_lengths, 4)))
+        return ATTN_ERR_MISALIGNED;
+
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    const int64_t num_qblocks = (static_cast<int64_t>(n) + 255) / 256;
+    if (bh > INT32_MAX || bh * num_qblocks > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (m == 0) {
+        const int64_t rows = bh * n;
+        const int64_t elems = rows * d_v;
+        const int64_t blocks = std::min<int64_t>((elems + 255) / 256, 152 * 8);
+        fill_no_keys_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+            static_cast<uint16_t*>(O), elems, LSE, rows);
+        cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? ATTN_OK : fail_cuda("fill kernel launch", e);
+    }
+
+    uint32_t* status = nullptr;
+    int rc = status_word(&status);
+    if (rc != ATTN_OK) return rc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    rc = encoder(&enc);
+    if (rc != ATTN_OK) return rc;
+
+    attn::TensorMaps maps;
+    if ((rc = make_map(enc, &maps.q, Q, bh, n, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.k, K, bh, m, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.v, V, bh, m, d_v, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.o, O, bh, n, d_v, 32)) != ATTN_OK) return rc;
+
+    const double sc = (scale > 0.f && std::isfinite(scale)) ? static_cast<double>(scale)
+                                                             : 1.0 / std::sqrt(static_cast<double>(d_k));
+    attn::FwdParams p;
+    p.B = B;
+    p.H = H;
+    p.n = n;
+    p.m = m;
+    p.num_qblocks = static_cast<int>(num_qblocks);
+    p.key_lengths = mask_kind == ATTN_MASK_KEY_PADDING ? key_lengths : nullptr;
+    p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
+    p.LSE = LSE;
+    p.status = status;
+    p.watchdog_ns = g_watchdog_ns;
+    p.debug_flags = g_debug_flags;
+
+    const int64_t ctas = bh * num_qblocks;
+    cudaError_t e = d_k == 64 ? attn::launch_fwd_d64(mask_kind, maps, p, ctas, st)
+                              : attn::launch_fwd_d128(mask_kind, maps, p, ctas, st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda("attention kernel launch", e);
+}
+
+int attn_get_device_status(void* stream, uint32_t* detail)
+{
+    uint32_t* status = nullptr;
+    int rc = status_word(&status);
+    if (rc != ATTN_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda("cudaStreamSynchronize", e);
+    uint32_t v = 0;
+    e = cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda("cudaMemcpy(status word)", e);
+    if (v != 0) {
+        e = cudaMemsetAsync(status, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(status word)", e);
+        e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail_cuda("cudaStreamSynchronize", e);
+    }
+    if (detail != nullptr) *detail = v;
+    return v != 0 ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+void attn_set_watchdog(uint64_t limit_ns, uint32_t debug_flags)
+{
+    g_watchdog_ns = limit_ns == 0 ? kDefaultWatchdogNs : limit_ns;
+    g_debug_flags = debug_flags;
+}
+
+const char* attn_status_string(int status)
+{
+    switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    default: return "ATTN_ERR_UNKNOWN";
+    }
+}
+
+const char* attn_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// attn_internal.h -- declarations shared by the host launcher (attn_api.cu) and
+// the kernel translation units. Not part of the public C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+enum { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_KEY_PADDING = 2 };
+
+// Bits of the device status word: which bounded wait gave up.
+enum : uint32_t {
+    STATUS_TMA_WAIT = 1u,      // producer waiting for a free K/V stage
+    STATUS_MMA_WAIT = 2u,      // MMA issuer waiting for data or for P
+    STATUS_SOFTMAX_WAIT = 4u,  // softmax/epilogue waiting for S or O
+    STATUS_FORCED = 8u,        // debug: wait on a barrier that nothing completes
+};
+
+enum : uint32_t { DEBUG_FORCE_TIMEOUT = 1u };
+
+struct FwdParams {
+    int B, H, n, m;
+    int num_qblocks;              // ceil(n / 256)
+    const int32_t* key_lengths;   // device int32 [B] (key padding only)
+    float scale_log2;             // scale * log2(e)
+    float* LSE;                   // fp32 [B,H,n] or null
+    uint32_t* status;             // device status word
+    uint64_t watchdog_ns;         // wall-clock limit of one bounded wait
+    uint32_t debug_flags;
+};
+
+struct TensorMaps {
+    CUtensorMap q, k, v, o;
+};
+
+cudaError_t launch_fwd_d64(int mask, const TensorMaps& maps, const FwdParams& p, int64_t num_ctas,
+                           cudaStream_t stream);
+cudaError_t launch_fwd_d128(int mask, const TensorMaps& maps, const FwdParams& p, int64_t num_ctas,
+                            cudaStream_t stream);
+
+}  // namespace attn
