@@ -169,8 +169,9 @@ def run_ours(args):
         with torch.cuda.graph(graph, stream=stream):
             for i in range(G):
                 step(i)
-    for _ in range(2):
-        graph.replay()
+    with torch.cuda.stream(stream):      # replay() launches on the current stream
+        for _ in range(2):
+            graph.replay()
     torch.cuda.synchronize(dev)
     reps = max(1, math.ceil(args.steps / G))
     K_steps = reps * G
@@ -182,10 +183,11 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter()
-        ev0.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        ev1.record(stream)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            ev1.record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
         if world > 1:
@@ -240,6 +242,9 @@ def run_ours(args):
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
     peak, peak_sus, hbm, src = peaks()
     kernel_tflops = flops / (ms * 1e-3) / 1e12
+    if kernel_tflops > 1.25 * peak or ms * K_steps < 0.5 * t_wall * 1e3 * 0.5:
+        raise RuntimeError(f"implausible timing: {kernel_tflops:.1f} TFLOP/s, device {ms * K_steps:.2f} ms "
+                           f"vs wall {t_wall * 1e3:.2f} ms")
 
     result = None
     if rank == 0:

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -107,7 +108,43 @@ __global__ void fill_no_keys_kernel(uint16_t* O, int64_t o_elems, float* LSE, in
         for (int64_t i = i0; i < rows; i += stride) LSE[i] = -INFINITY;
 }
 
+// Number of SMs of the current device (cached per device).
+int sm_count(int* out)
+{
+    static int cached[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return fail_msg("device index out of range");
+    if (cached[dev] == 0) {
+        int v = 0;
+        e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail_cuda("cudaDeviceGetAttribute", e);
+        cached[dev] = v;
+    }
+    *out = cached[dev];
+    return ATTN_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Kernel variant per head dim. Defaults: one tile per CTA with P apart from S
+// (KERNEL_DP) at both d = 64 and d = 128. ATTN_KERNEL=dp|nt1|nt2 overrides it
+// (a tuning knob for measurements, read once).
+int kernel_variant(int d)
+{
+    static int env = [] {
+        const char* v = std::getenv("ATTN_KERNEL");
+        if (v == nullptr) return -1;
+        if (std::strcmp(v, "dp") == 0) return static_cast<int>(attn::KERNEL_DP);
+        if (std::strcmp(v, "nt1") == 0) return static_cast<int>(attn::KERNEL_NT1);
+        if (std::strcmp(v, "nt2") == 0) return static_cast<int>(attn::KERNEL_NT2);
+        return -1;
+    }();
+    if (env >= 0) return env;
+    (void)d;
+    return attn::KERNEL_DP;
+}
 
 }  // namespace
 
@@ -131,7 +168,9 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
         return ATTN_ERR_MISALIGNED;
 
     const int64_t bh = static_cast<int64_t>(B) * H;
-    const int64_t num_qblocks = (static_cast<int64_t>(n) + 255) / 256;
+    const int variant = kernel_variant(d_k);
+    const int64_t rows_per_cta = attn::kernel_rows_per_cta(variant);
+    const int64_t num_qblocks = (static_cast<int64_t>(n) + rows_per_cta - 1) / rows_per_cta;
     if (bh > INT32_MAX || bh * num_qblocks > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -166,6 +205,9 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
     p.n = n;
     p.m = m;
     p.num_qblocks = static_cast<int>(num_qblocks);
+    p.num_units = static_cast<int>(
+        bh * (variant == attn::KERNEL_DP && mask_kind == ATTN_MASK_CAUSAL ? (num_qblocks + 1) / 2 : num_qblocks));
+    p.O = O;
     p.key_lengths = mask_kind == ATTN_MASK_KEY_PADDING ? key_lengths : nullptr;
     p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
     p.LSE = LSE;
@@ -173,9 +215,11 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
     p.watchdog_ns = g_watchdog_ns;
     p.debug_flags = g_debug_flags;
 
+    int num_sms = 0;
+    if ((rc = sm_count(&num_sms)) != ATTN_OK) return rc;
     const int64_t ctas = bh * num_qblocks;
-    cudaError_t e = d_k == 64 ? attn::launch_fwd_d64(mask_kind, maps, p, ctas, st)
-                              : attn::launch_fwd_d128(mask_kind, maps, p, ctas, st);
+    cudaError_t e = d_k == 64 ? attn::launch_fwd_d64(mask_kind, variant, maps, p, ctas, num_sms, st)
+                              : attn::launch_fwd_d128(mask_kind, variant, maps, p, ctas, num_sms, st);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("attention kernel launch", e);
 }
 

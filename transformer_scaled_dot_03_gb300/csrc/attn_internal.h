@@ -22,7 +22,9 @@ enum : uint32_t { DEBUG_FORCE_TIMEOUT = 1u };
 
 struct FwdParams {
     int B, H, n, m;
-    int num_qblocks;              // ceil(n / 256)
+    int num_qblocks;              // ceil(n / rows per work unit)
+    int num_units;                // B * H * num_qblocks (persistent kernel)
+    void* O;                      // bf16 [B,H,n,d_v] (persistent kernel stores rows directly)
     const int32_t* key_lengths;   // device int32 [B] (key padding only)
     float scale_log2;             // scale * log2(e)
     float* LSE;                   // fp32 [B,H,n] or null
@@ -35,9 +37,18 @@ struct TensorMaps {
     CUtensorMap q, k, v, o;
 };
 
-cudaError_t launch_fwd_d64(int mask, const TensorMaps& maps, const FwdParams& p, int64_t num_ctas,
-                           cudaStream_t stream);
-cudaError_t launch_fwd_d128(int mask, const TensorMaps& maps, const FwdParams& p, int64_t num_ctas,
-                            cudaStream_t stream);
+// Kernel variants (see the kernel headers):
+//   KERNEL_DP   one query tile per CTA, P apart from S in tensor memory
+//   KERNEL_NT1  one query tile per CTA, P over S
+//   KERNEL_NT2  two query tiles per CTA, P over S
+enum { KERNEL_DP = 0, KERNEL_NT1 = 1, KERNEL_NT2 = 2 };
+
+inline int kernel_rows_per_cta(int variant) { return variant == KERNEL_NT2 ? 256 : 128; }
+
+// num_ctas: grid of the one-unit-per-CTA variants; num_sms sizes the persistent grid.
+cudaError_t launch_fwd_d64(int mask, int variant, const TensorMaps& maps, const FwdParams& p,
+                           int64_t num_ctas, int num_sms, cudaStream_t stream);
+cudaError_t launch_fwd_d128(int mask, int variant, const TensorMaps& maps, const FwdParams& p,
+                            int64_t num_ctas, int num_sms, cudaStream_t stream);
 
 }  // namespace attn

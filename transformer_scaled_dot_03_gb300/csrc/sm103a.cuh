@@ -320,6 +320,22 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
         : "memory");
 }
 
+// ------------------------------------------------------------------ registers
+
+// Re-balance the per-thread register budget between warpgroups (all four warps
+// of a warpgroup execute the same instruction).
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------------ arithmetic
 
 __device__ __forceinline__ float ex2_approx(float x)
