@@ -87,7 +87,7 @@ struct Layout {
     static constexpr uint32_t TMEM_COLS = D == 64 ? 256 : 512;
     static constexpr uint32_t S_COL = 0, P_COL = 128, O_COL = 192, QT_COL = 192 + D;
     static constexpr uint32_t REG_LAUNCH = (65536 / (NUM_THREADS * CTAS_PER_SM)) / 8 * 8;
-    static constexpr uint32_t REG_CTRL = 56;
+    static constexpr uint32_t REG_CTRL = 72;
     static constexpr uint32_t REG_SOFTMAX_FIT = ((REG_LAUNCH * NUM_THREADS - REG_CTRL * 128) / 128) / 8 * 8;
     static constexpr uint32_t REG_SOFTMAX = REG_SOFTMAX_FIT > 248 ? 248 : REG_SOFTMAX_FIT;
     static_assert(128 * REG_SOFTMAX + 128 * REG_CTRL <= REG_LAUNCH * NUM_THREADS, "register split");
@@ -286,48 +286,52 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 drain_wait(bar(L::B_KFULL + i % L::KS), static_cast<uint32_t>(i / L::KS) & 1u, 100000000ull);
             for (int i = vc - 1; i >= 0 && i >= vc - L::VS; --i)
                 drain_wait(bar(L::B_VFULL + i % L::VS), static_cast<uint32_t>(i / L::VS) & 1u, 100000000ull);
-        } else if (warp == L::WARP_MMA && lane == 0) {
+        } else if (warp == L::WARP_MMA) {
             // ================================================== MMA issuer
+            // The whole warp runs this loop with warp-uniform values; one elected
+            // lane issues each tcgen05 instruction. Descriptors are formed once per
+            // buffer and advanced by adding the encoded byte offset (address >> 4).
             constexpr uint32_t ID_S = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t ID_PV = idesc_bf16_f32(BM, D, false, true);
+            const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
+            const uint64_t dV0 = sdesc_sw128(sV, CHUNK_BYTES, 1024);
             int qc = 0, kc = 0, vc = 0, g = 0;   // g: key-tile steps over all tiles
+            auto wait = [&](int b, uint32_t parity) -> bool {
+                const bool r = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_MMA_WAIT, limit);
+                return __all_sync(0xffffffffu, r);
+            };
             auto issue_S = [&](int s) {
-                const uint32_t b0 = sK + s * L::TILE;
+                const uint64_t dK = dK0 + static_cast<uint64_t>((s * L::TILE) >> 4);
                 const uint32_t qt = tmem + L::QT_COL + static_cast<uint32_t>((qc - 1) & 1) * (D / 2);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * CHUNK_BYTES + (kk % 4) * 32;
+                    const uint64_t off = static_cast<uint64_t>(((kk / 4) * CHUNK_BYTES + (kk % 4) * 32) >> 4);
                     if (L::Q_IN_TMEM)
-                        mma_ts(tmem + L::S_COL, qt + kk * 8, sdesc_sw128(b0 + off, 16, 1024), ID_S,
-                               kk > 0 ? 1u : 0u);
+                        mma_ts_warp(tmem + L::S_COL, qt + kk * 8, dK + off, ID_S, kk > 0 ? 1u : 0u);
                     else
-                        mma_ss(tmem + L::S_COL, sdesc_sw128(sQ + off, 16, 1024),
-                               sdesc_sw128(b0 + off, 16, 1024), ID_S, kk > 0 ? 1u : 0u);
+                        mma_ss_warp(tmem + L::S_COL, dQ + off, dK + off, ID_S, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_PV = [&](int s, bool acc) {
-                const uint32_t v0 = sV + s * L::TILE;
+                const uint64_t dV = dV0 + static_cast<uint64_t>((s * L::TILE) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(tmem + L::O_COL, tmem + L::P_COL + kk * 8,
-                           sdesc_sw128(v0 + kk * 2048, CHUNK_BYTES, 1024), ID_PV, (acc || kk > 0) ? 1u : 0u);
+                    mma_ts_warp(tmem + L::O_COL, tmem + L::P_COL + kk * 8, dV + static_cast<uint64_t>((kk * 2048) >> 4),
+                                ID_PV, (acc || kk > 0) ? 1u : 0u);
             };
             bool ok = true;
             // S(g) for the key tile in ring slot kc; waits for the data and for the
             // softmax to have loaded S(g-1) out of the S columns.
             auto next_S = [&](bool last_of_tile) -> bool {
                 const int s = kc % L::KS;
-                if (!mbar_wait(bar(L::B_KFULL + s), static_cast<uint32_t>(kc / L::KS) & 1u, abort_word, p.status,
-                               STATUS_MMA_WAIT, limit))
-                    return false;
-                if (g > 0 && !mbar_wait(bar(L::B_SFREE), static_cast<uint32_t>(g - 1) & 1u, abort_word,
-                                        p.status, STATUS_MMA_WAIT, limit))
-                    return false;
+                if (!wait(L::B_KFULL + s, static_cast<uint32_t>(kc / L::KS) & 1u)) return false;
+                if (g > 0 && !wait(L::B_SFREE, static_cast<uint32_t>(g - 1) & 1u)) return false;
                 tc_fence_after();
                 issue_S(s);
-                mma_commit(bar(L::B_SFULL));
-                mma_commit(bar(L::B_KEMPTY + s));
-                if (last_of_tile && !L::Q_IN_TMEM) mma_commit(bar(L::B_QFREE));
+                mma_commit_warp(bar(L::B_SFULL));
+                mma_commit_warp(bar(L::B_KEMPTY + s));
+                if (last_of_tile && !L::Q_IN_TMEM) mma_commit_warp(bar(L::B_QFREE));
                 ++kc;
                 ++g;
                 return true;
@@ -335,8 +339,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             for (TilePos t = first_tile; ok && t.u < p.num_units; advance<MASK>(t, u_step, p)) {
                 const Unit w = tile_of<MASK>(t.u, t.ti, p);
                 if (w.nkv == 0) continue;
-                ok = mbar_wait(bar(L::Q_IN_TMEM ? L::B_QREADY : L::B_QFULL), static_cast<uint32_t>(qc) & 1u,
-                               abort_word, p.status, STATUS_MMA_WAIT, limit);
+                ok = wait(L::Q_IN_TMEM ? L::B_QREADY : L::B_QFULL, static_cast<uint32_t>(qc) & 1u);
                 ++qc;
                 if (ok) ok = next_S(w.nkv == 1);
                 for (int j = 0; ok && j < w.nkv; ++j) {
@@ -346,19 +349,17 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     }
                     const int sv = vc % L::VS;
                     const int step = g - (j + 1 < w.nkv ? 2 : 1);   // this tile's step j
-                    ok = mbar_wait(bar(L::B_VFULL + sv), static_cast<uint32_t>(vc / L::VS) & 1u, abort_word,
-                                   p.status, STATUS_MMA_WAIT, limit) &&
-                         mbar_wait(bar(L::B_PFULL), static_cast<uint32_t>(step) & 1u, abort_word, p.status,
-                                   STATUS_MMA_WAIT, limit);
+                    ok = wait(L::B_VFULL + sv, static_cast<uint32_t>(vc / L::VS) & 1u) &&
+                         wait(L::B_PFULL, static_cast<uint32_t>(step) & 1u);
                     if (!ok) break;
                     tc_fence_after();
                     issue_PV(sv, j > 0);
-                    mma_commit(bar(L::B_PVDONE));
-                    mma_commit(bar(L::B_VEMPTY + sv));
+                    mma_commit_warp(bar(L::B_PVDONE));
+                    mma_commit_warp(bar(L::B_VEMPTY + sv));
                     ++vc;
                 }
             }
-            mma_commit(bar(L::B_DRAIN));
+            mma_commit_warp(bar(L::B_DRAIN));
             drain_wait(bar(L::B_DRAIN), 0, 100000000ull);
         }
         __syncwarp();
