@@ -444,8 +444,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                 for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
                 const int key0 = j * BN;
-                const bool need_mask =
-                    (key0 + BN > w.kv_len) || (MASK == MASK_CAUSAL && key0 + BN - 1 > qrow);
+                const bool need_mask = __any_sync(
+                    0xffffffffu, (key0 + BN > w.kv_len) || (MASK == MASK_CAUSAL && key0 + BN - 1 > qrow));
                 if (need_mask) {
 #pragma unroll
                     for (int c = 0; c < BN; ++c) {
@@ -453,34 +453,40 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         if (key >= w.kv_len || (MASK == MASK_CAUSAL && key > qrow)) s[c] = -INFINITY;
                     }
                 }
+                // row maximum: eight independent chains of three-input max
                 float mx[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) mx[k] = s[k];
+                for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[2 * k], s[2 * k + 1]);
 #pragma unroll
-                for (int c = 8; c < BN; c += 8)
+                for (int c = 16; c < BN; c += 16)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[c + k]);
+                    for (int k = 0; k < 8; ++k) mx[k] = max3f(mx[k], s[c + 2 * k], s[c + 2 * k + 1]);
                 const float tile_max =
-                    fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                          fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+                    max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
                 const bool raise = tile_max > m_ref + RESCALE_LOG2;
                 const float m_new = raise ? tile_max : m_ref;
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                 const float alpha = raise ? ex2_approx(m_ref - m_use) : 1.f;
 
+                // p = exp2(s * scale*log2e - m) on score pairs (packed fp32 arithmetic)
+                const uint64_t sl22 = f2_pack(sl2, sl2);
+                const uint64_t nm2 = f2_pack(-m_use, -m_use);
                 uint32_t pk[BN / 2];
-                float rs[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) rs[k] = 0.f;
+                uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < BN / 2; ++c) {
-                    const float p0 = ex2_approx(fmaf(s[2 * c], sl2, -m_use));
-                    const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -m_use));
-                    rs[c % 8] += p0 + p1;
+                    const uint64_t x2 = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl22, nm2);
+                    float a, b;
+                    f2_unpack(x2, a, b);
+                    const uint64_t p2 = f2_pack(ex2_approx(a), ex2_approx(b));
+                    rs2[c % 4] = f2_add(rs2[c % 4], p2);
+                    float p0, p1;
+                    f2_unpack(p2, p0, p1);
                     pk[c] = pack_bf16x2(p0, p1);
                 }
-                l_run = l_run * alpha +
-                        (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
+                float r0, r1;
+                f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])), r0, r1);
+                l_run = l_run * alpha + (r0 + r1);
 
                 if (g > 0) {
                     // the previous O += P V must be complete: it reads the P columns,
