@@ -103,6 +103,35 @@ int attn_get_device_status(void* stream, uint32_t* detail);
  */
 void attn_set_watchdog(uint64_t limit_ns, uint32_t debug_flags);
 
+/*
+ * attn_fwd without device memory allocation. The pages have no counterpart to
+ * this entry point; it exists for callers that may not call cudaMalloc, such
+ * as code running while another component owns every device allocation (a
+ * pooled or caching allocator, a fixed memory budget) or code that must not
+ * add device allocations once it is running.
+ *
+ * Arguments, layouts, results and status codes are those of attn_fwd. The
+ * difference is the kernel's scratch memory: attn_fwd allocates its 4-byte
+ * device status word on first use, while this entry point takes its scratch
+ * from a fixed 256-byte device array inside the library (every GPU that loads
+ * the library keeps it until the process exits). One call needs 4 bytes of it
+ * whatever the problem sizes; a need beyond the 256 bytes would be refused
+ * with ATTN_ERR_UNSUPPORTED. No call allocates or frees device memory.
+ *
+ *   - The first call on each device looks up the array's device address (a
+ *     cudaGetSymbolAddress on that device); make that first call before any
+ *     stream capture on the device.
+ *   - All calls share the array. Each call resets the status word to zero on
+ *     `stream` before its kernel, so calls whose kernels overlap on the GPU
+ *     (different streams, no ordering between them) race on it.
+ *   - A device-side watchdog expiry is recorded in the shared array only; it
+ *     is not reported by attn_get_device_status. Use attn_fwd when that report
+ *     is needed.
+ */
+int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+                     int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O,
+                     float* LSE, void* stream);
+
 /* Human-readable name of a status code. */
 const char* attn_status_string(int status);
 

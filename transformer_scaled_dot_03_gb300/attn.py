@@ -32,7 +32,7 @@ MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PAD
 
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
-           "attn_last_error")
+           "attn_last_error", "attn_fwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None

@@ -265,3 +265,125 @@ const char* attn_status_string(int status)
 const char* attn_last_error(void) { return g_last_error; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that may not allocate device memory.
+//
+// attn_fwd keeps its device status word (the kernel's only scratch memory) in
+// a 4-byte cudaMalloc made on the first call on each device. Some callers
+// cannot allow that: code that runs while another component owns every
+// allocation (a caching or pooled allocator, a fixed memory budget), or code
+// that must not add device allocations after start-up. attn_fwd_noalloc runs
+// the same kernel with its scratch taken from this file-scope device array.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256;                  // stated maximum
+constexpr size_t kNoAllocStatusBytes = sizeof(uint32_t);      // scratch one call needs
+static_assert(kNoAllocStatusBytes <= kNoAllocScratchBytes, "scratch layout");
+
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint32_t)];
+
+std::mutex g_noalloc_mu;
+uint32_t* g_noalloc_addr[kMaxDevices] = {};   // device address of the array, per device
+
+// Device address of the scratch array on the current device, looked up once
+// per device. In host code the array's name is only a host-side stand-in.
+int noalloc_scratch(uint32_t** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return fail_msg("device index out of range");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return fail_cuda("cudaGetSymbolAddress(no-allocation scratch)", e);
+        if (ptr == nullptr) return fail_msg("no-allocation scratch has no device address");
+        g_noalloc_addr[dev] = static_cast<uint32_t*>(ptr);
+    }
+    *out = g_noalloc_addr[dev];
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int B, int H, int n, int m,
+                                int d_k, int d_v, int mask_kind, const int32_t* key_lengths, float scale,
+                                void* O, float* LSE, void* stream)
+{
+    if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind == ATTN_MASK_CAUSAL && n != m) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind == ATTN_MASK_KEY_PADDING && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!(d_k == d_v && (d_k == 64 || d_k == 128))) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || n == 0) return ATTN_OK;
+    if (O == nullptr || (m > 0 && (Q == nullptr || K == nullptr || V == nullptr))) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(O, 16) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return ATTN_ERR_MISALIGNED;
+    if ((LSE != nullptr && !aligned(LSE, 4)) || (key_lengths != nullptr && !aligned(key_lengths, 4)))
+        return ATTN_ERR_MISALIGNED;
+
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    const int variant = kernel_variant(d_k);
+    const int64_t rows_per_cta = attn::kernel_rows_per_cta(variant);
+    const int64_t num_qblocks = (static_cast<int64_t>(n) + rows_per_cta - 1) / rows_per_cta;
+    if (bh > INT32_MAX || bh * num_qblocks > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    // The kernel's scratch for one call is the status word, whatever the sizes;
+    // anything larger than the array would be refused here.
+    if (kNoAllocStatusBytes > kNoAllocScratchBytes) {
+        snprintf(g_last_error, sizeof(g_last_error), "attn_fwd_noalloc: scratch need %zu B exceeds %zu B",
+                 kNoAllocStatusBytes, kNoAllocScratchBytes);
+        return ATTN_ERR_UNSUPPORTED;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (m == 0) {
+        const int64_t rows = bh * n;
+        const int64_t elems = rows * d_v;
+        const int64_t blocks = std::min<int64_t>((elems + 255) / 256, 152 * 8);
+        fill_no_keys_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint16_t*>(O), elems,
+                                                                           LSE, rows);
+        cudaError_t e = cudaGetLastError();
+        return e == cudaSuccess ? ATTN_OK : fail_cuda("fill kernel launch", e);
+    }
+
+    uint32_t* scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc != ATTN_OK) return rc;
+    // the status word must start at zero; it keeps the previous call's value otherwise
+    cudaError_t e = cudaMemsetAsync(scratch, 0, kNoAllocStatusBytes, st);
+    if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(no-allocation scratch)", e);
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    if ((rc = encoder(&enc)) != ATTN_OK) return rc;
+
+    attn::TensorMaps maps;
+    if ((rc = make_map(enc, &maps.q, Q, bh, n, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.k, K, bh, m, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.v, V, bh, m, d_v, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.o, O, bh, n, d_v, 32)) != ATTN_OK) return rc;
+
+    const double sc = (scale > 0.f && std::isfinite(scale)) ? static_cast<double>(scale)
+                                                             : 1.0 / std::sqrt(static_cast<double>(d_k));
+    attn::FwdParams p;
+    p.B = B;
+    p.H = H;
+    p.n = n;
+    p.m = m;
+    p.num_qblocks = static_cast<int>(num_qblocks);
+    p.num_units = static_cast<int>(
+        bh * (variant == attn::KERNEL_DP && mask_kind == ATTN_MASK_CAUSAL ? (num_qblocks + 1) / 2 : num_qblocks));
+    p.O = O;
+    p.key_lengths = mask_kind == ATTN_MASK_KEY_PADDING ? key_lengths : nullptr;
+    p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
+    p.LSE = LSE;
+    p.status = scratch;
+    p.watchdog_ns = g_watchdog_ns;
+    p.debug_flags = g_debug_flags;
+
+    int num_sms = 0;
+    if ((rc = sm_count(&num_sms)) != ATTN_OK) return rc;
+    const int64_t ctas = bh * num_qblocks;
+    e = d_k == 64 ? attn::launch_fwd_d64(mask_kind, variant, maps, p, ctas, num_sms, st)
+                  : attn::launch_fwd_d128(mask_kind, variant, maps, p, ctas, num_sms, st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda("attention kernel launch", e);
+}
