@@ -16,14 +16,21 @@
  *           none         every j                     (encoder self-attention,
  *                                                     "Transformer 详解" §4.1;
  *                                                     cross-attention §5.4)
- *           causal       j <= i                      ("Transformer 详解" §5.3
+ *           causal       j <= i + (m - n)            ("Transformer 详解" §5.3
  *                                                     Mask_ij = 0 if j<=i else
  *                                                     -inf; "第2章：完整的
- *                                                     Transformer 架构" §6)
+ *                                                     Transformer 架构" §6; the
+ *                                                     pages give the square
+ *                                                     case n = m; for n != m
+ *                                                     the queries are the last
+ *                                                     n positions of the m keys)
  *           key padding  j < len_b, all query rows   ("Transformer 详解" §3.4:
  *                                                     mask [batch,1,1,seq]
  *                                                     broadcasts over heads and
  *                                                     queries, masks keys)
+ *           causal and   both conditions             ("Transformer 详解" §5.3:
+ *           key padding                               tgt_mask = pad_mask &
+ *                                                     subsequent_mask)
  *   mu    = max_{j in J} s_j;  Z = sum_{j in J} exp(s_j - mu)
  *   w_j   = exp(s_j - mu) / Z for j in J, 0 otherwise      (row softmax; the
  *           shift by mu leaves the value unchanged and keeps exp in range)
@@ -36,13 +43,12 @@
  * "Transformer 详解" §3.4 gives the same result in fp64. A row with no
  * visible key (key length 0) gets o_i = 0 and LSE_i = -inf.
  *
- * Key lengths are clamped to [0, m]. Causal masking is defined for any n, m
- * here as j <= i (the pages only print the square case).
+ * Key lengths are clamped to [0, m].
  *
  * Layouts: Q [B,H,n,dk], K [B,H,m,dk], V [B,H,m,dv], O [B,H,n,dv], LSE
  * [B,H,n], all contiguous row-major fp64; key_lengths int32 [B].
  *
- * ORACLE_PLANT (compile-time, default 0) plants one known mistake so that the
+ * ORACLE_PLANT (compile-time, default 0, 1..8) plants one known mistake so that the
  * test suite can show that its pins catch it; the shipped build never sets it.
  */
 #include <math.h>
@@ -55,32 +61,61 @@
 #define ORACLE_PLANT 0
 #endif
 
-enum { ORACLE_MASK_NONE = 0, ORACLE_MASK_CAUSAL = 1, ORACLE_MASK_KEY_PADDING = 2 };
+enum {
+    ORACLE_MASK_NONE = 0,
+    ORACLE_MASK_CAUSAL = 1,
+    ORACLE_MASK_KEY_PADDING = 2,
+    ORACLE_MASK_CAUSAL_KEY_PADDING = 3
+};
 
-/* Is key j visible to query row i? */
-static int visible(int mask_kind, int64_t i, int64_t j, int64_t len)
+static int causal_visible(int64_t i, int64_t j, int64_t off)
+{
+#if ORACLE_PLANT == 2
+    return j < i + off;            /* planted: diagonal excluded */
+#elif ORACLE_PLANT == 7
+    (void)off;
+    return j <= i;                 /* planted: diagonal not shifted for n != m */
+#else
+    return j <= i + off;
+#endif
+}
+
+static int padding_visible(int64_t i, int64_t j, int64_t len)
+{
+#if ORACLE_PLANT == 5
+    (void)j;
+    return i < len;                /* planted: padding applied to queries */
+#else
+    (void)i;
+    return j < len;
+#endif
+}
+
+/* Is key j visible to query row i? off = m - n aligns the causal diagonal so
+ * that the last query row sees every key. */
+static int visible(int mask_kind, int64_t i, int64_t j, int64_t len, int64_t off)
 {
     switch (mask_kind) {
-    case ORACLE_MASK_CAUSAL:
-#if ORACLE_PLANT == 2
-        return j < i;              /* planted: diagonal excluded */
+    case ORACLE_MASK_CAUSAL: return causal_visible(i, j, off);
+    case ORACLE_MASK_KEY_PADDING: return padding_visible(i, j, len);
+    case ORACLE_MASK_CAUSAL_KEY_PADDING:
+#if ORACLE_PLANT == 8
+        return causal_visible(i, j, off) || padding_visible(i, j, len);  /* planted: union */
 #else
-        return j <= i;
+        return causal_visible(i, j, off) && padding_visible(i, j, len);
 #endif
-    case ORACLE_MASK_KEY_PADDING:
-#if ORACLE_PLANT == 5
-        return i < len;            /* planted: padding applied to queries */
-#else
-        return j < len;
-#endif
-    default:
-        return 1;
+    default: return 1;
     }
+}
+
+static int uses_lengths(int mask_kind)
+{
+    return mask_kind == ORACLE_MASK_KEY_PADDING || mask_kind == ORACLE_MASK_CAUSAL_KEY_PADDING;
 }
 
 static int64_t clamp_len(const int32_t* key_lengths, int mask_kind, int64_t b, int64_t m)
 {
-    if (mask_kind != ORACLE_MASK_KEY_PADDING || key_lengths == NULL) return m;
+    if (!uses_lengths(mask_kind) || key_lengths == NULL) return m;
     int64_t len = key_lengths[b];
     if (len < 0) len = 0;
     if (len > m) len = m;
@@ -93,8 +128,8 @@ static int64_t clamp_len(const int32_t* key_lengths, int mask_kind, int64_t b, i
  * is not NULL, the m attention weights of the row.
  */
 static void attn_row(const double* q, const double* Kh, const double* Vh, int64_t m,
-                     int dk, int dv, int mask_kind, int64_t i, int64_t len, double scale,
-                     double* s, double* o, double* lse, double* w_out)
+                     int dk, int dv, int mask_kind, int64_t i, int64_t len, int64_t off,
+                     double scale, double* s, double* o, double* lse, double* w_out)
 {
     /* 1. scaled scores of every key */
     for (int64_t j = 0; j < m; ++j) {
@@ -116,7 +151,7 @@ static void attn_row(const double* q, const double* Kh, const double* Vh, int64_
     double mu = -INFINITY;
     int64_t count = 0;
     for (int64_t j = 0; j < m; ++j) {
-        if (!visible(mask_kind, i, j, len)) continue;
+        if (!visible(mask_kind, i, j, len, off)) continue;
         if (s[j] > mu) mu = s[j];
         ++count;
     }
@@ -129,9 +164,9 @@ static void attn_row(const double* q, const double* Kh, const double* Vh, int64_
     /* 3. normaliser and weights */
     double Z = 0.0;
     for (int64_t j = 0; j < m; ++j)
-        if (visible(mask_kind, i, j, len)) Z += exp(s[j] - mu);
+        if (visible(mask_kind, i, j, len, off)) Z += exp(s[j] - mu);
     for (int64_t j = 0; j < m; ++j) {
-        double wj = visible(mask_kind, i, j, len) ? exp(s[j] - mu) / Z : 0.0;
+        double wj = visible(mask_kind, i, j, len, off) ? exp(s[j] - mu) / Z : 0.0;
 #if ORACLE_PLANT == 6
         if (j == 0) wj = 0.0;      /* planted: first key dropped from the sum */
 #endif
@@ -178,7 +213,7 @@ static void* worker(void* arg)
             for (int64_t i = 0; i < jb->n; ++i) {
                 int64_t r = bh * jb->n + i;
                 attn_row(jb->Q + r * jb->dk, Kh, Vh, jb->m, jb->dk, jb->dv, jb->mask_kind, i,
-                         len, jb->scale, s, jb->O + r * jb->dv, jb->LSE + r,
+                         len, jb->m - jb->n, jb->scale, s, jb->O + r * jb->dv, jb->LSE + r,
                          jb->W ? jb->W + r * jb->m : NULL);
             }
         }
@@ -190,7 +225,7 @@ static void* worker(void* arg)
             int64_t len = clamp_len(jb->key_lengths, jb->mask_kind, b, jb->m);
             attn_row(jb->Q + r * jb->dk, jb->K + bh * jb->m * jb->dk,
                      jb->V + bh * jb->m * jb->dv, jb->m, jb->dk, jb->dv, jb->mask_kind, i, len,
-                     jb->scale, s, jb->O + k * jb->dv, jb->LSE + k, NULL);
+                     jb->m - jb->n, jb->scale, s, jb->O + k * jb->dv, jb->LSE + k, NULL);
         }
     }
     free(s);
@@ -226,7 +261,7 @@ static int run(job_t base)
 static int bad_args(int64_t B, int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind)
 {
     return B < 0 || H < 0 || n < 0 || m < 0 || dk < 1 || dv < 1 || mask_kind < 0 ||
-           mask_kind > 2;
+           mask_kind > 3;
 }
 
 /* Full forward: O [B,H,n,dv] and LSE [B,H,n]. W (optional, [B,H,n,m]) gets the
@@ -237,7 +272,7 @@ int oracle_attn_fwd(const double* Q, const double* K, const double* V, int64_t B
                     double* W, int nthreads)
 {
     if (bad_args(B, H, n, m, dk, dv, mask_kind)) return -1;
-    if (mask_kind == ORACLE_MASK_KEY_PADDING && key_lengths == NULL) return -1;
+    if (uses_lengths(mask_kind) && key_lengths == NULL) return -1;
     job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, O, LSE, W,
                 NULL, 0, nthreads, 0};
     return run(jb);
@@ -251,7 +286,7 @@ int oracle_attn_rows(const double* Q, const double* K, const double* V, int64_t 
                      int64_t nrows, double* O, double* LSE, int nthreads)
 {
     if (bad_args(B, H, n, m, dk, dv, mask_kind) || rows == NULL || nrows < 0) return -1;
-    if (mask_kind == ORACLE_MASK_KEY_PADDING && key_lengths == NULL) return -1;
+    if (uses_lengths(mask_kind) && key_lengths == NULL) return -1;
     for (int64_t k = 0; k < nrows; ++k)
         if (rows[k] < 0 || rows[k] >= B * H * n) return -1;
     job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, O, LSE, NULL,

@@ -4,7 +4,9 @@ Every pin is a function ``pin_*(plant)`` that raises AssertionError on a
 mismatch. The tests run each pin on the shipped oracle (plant 0), and then
 rebuild the oracle with each planted mistake (a dropped scale, a wrong causal
 boundary, a wrong K index, a missing max shift in the LSE, padding applied to
-queries, a dropped key) and require that at least one pin catches it.
+queries, a dropped key, a causal diagonal not shifted for n != m, a union in
+place of the intersection of the two masks) and require that at least one pin
+catches it.
 """
 
 import math
@@ -187,15 +189,15 @@ def pin_fill_minus_1e9(plant=0):
 
 
 def _torch_ref(Q, K, V, mask, lens, scale):
+    """Library reference for cases where every row sees at least one key."""
     q, k, v = map(torch.from_numpy, (Q, K, V))
     B, H, n, d = q.shape
     m = k.shape[2]
-    if mask == "causal":
-        allowed = torch.ones(n, m, dtype=torch.bool).tril()
-    elif mask == "key_padding":
-        allowed = (torch.arange(m)[None, :] < torch.tensor(lens)[:, None]).view(B, 1, 1, m)
-    else:
-        allowed = torch.ones(n, m, dtype=torch.bool)
+    allowed = torch.ones(1, 1, n, m, dtype=torch.bool)
+    if mask in ("causal", "causal_key_padding"):
+        allowed = allowed & torch.ones(n, m, dtype=torch.bool).tril(diagonal=m - n)
+    if mask in ("key_padding", "causal_key_padding"):
+        allowed = allowed & (torch.arange(m)[None, :] < torch.tensor(lens)[:, None]).view(B, 1, 1, m)
     O = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=allowed, scale=scale)
     s = torch.matmul(q, k.transpose(-1, -2)) * scale
     L = torch.logsumexp(s.masked_fill(~allowed, float("-inf")), dim=-1)
@@ -212,6 +214,9 @@ def pin_library_brute_force(plant=0):
         (2, 2, 9, 9, 2, 3, "causal", None, None),
         (3, 1, 5, 12, 8, 8, "key_padding", [1, 12, 7], None),
         (2, 2, 16, 13, 64, 16, "key_padding", [13, 2], 0.7),
+        (2, 2, 4, 11, 8, 8, "causal", None, None),
+        (2, 1, 7, 7, 8, 4, "causal_key_padding", [7, 3], None),
+        (3, 2, 5, 9, 16, 16, "causal_key_padding", [9, 6, 5], None),
     ]
     for t, (B, H, n, m, dk, dv, mask, lens, sc) in enumerate(cases):
         Q, K, V = rnd((B, H, n, dk), 100 + t), rnd((B, H, m, dk), 200 + t), rnd((B, H, m, dv), 300 + t)
@@ -234,9 +239,53 @@ def pin_two_key_logistic(plant=0):
         assert abs(L[0, 0, 0] - (a + math.log1p(math.exp(-delta)))) < 1e-9 * max(1.0, abs(a))
 
 
+def pin_causal_suffix(plant=0):
+    """Causal attention of n < m queries is the last n rows of the square causal
+    self-attention over all m positions ("Transformer 详解" §5.3: row i sees the keys up
+    to its own position; the n queries are the last n positions). The square case is
+    pinned by the page's 3x3 example and by causal row 0."""
+    B, H, m, d = 2, 2, 13, 8
+    Qf, K, V = rnd((B, H, m, d), 30), rnd((B, H, m, d), 31), rnd((B, H, m, 6), 32)
+    Of, Lf = oracle.attn_fwd(Qf, K, V, "causal", plant=plant)
+    for n in (1, 4, 12):
+        O, L = oracle.attn_fwd(Qf[:, :, m - n:], K, V, "causal", plant=plant)
+        np.testing.assert_allclose(O, Of[:, :, m - n:], atol=1e-12)
+        np.testing.assert_allclose(L, Lf[:, :, m - n:], atol=1e-12)
+    # a single query (n = 1) therefore sees every key: plain unmasked attention
+    O1, L1 = oracle.attn_fwd(Qf[:, :, -1:], K, V, "causal", plant=plant)
+    On, Ln = oracle.attn_fwd(Qf[:, :, -1:], K, V, "none", plant=plant)
+    np.testing.assert_allclose(O1, On, atol=1e-12)
+    np.testing.assert_allclose(L1, Ln, atol=1e-12)
+
+
+def pin_causal_and_padding(plant=0):
+    """The decoder target mask is the intersection of the padding mask and the causal mask
+    ("Transformer 详解" §5.3). Row i then sees keys j <= min(i + m - n, len - 1): it equals
+    the causal result while i + m - n < len and the key-padding result once
+    i + m - n >= len - 1; with len = m it is the causal mask itself."""
+    B, H, n, m, d = 3, 2, 9, 12, 8
+    Q, K, V = rnd((B, H, n, d), 33), rnd((B, H, m, d), 34), rnd((B, H, m, 5), 35)
+    lens = [12, 7, 4]
+    O, L = oracle.attn_fwd(Q, K, V, "causal_key_padding", key_lengths=lens, plant=plant)
+    Oc, Lc = oracle.attn_fwd(Q, K, V, "causal", plant=plant)
+    Op, Lp = oracle.attn_fwd(Q, K, V, "key_padding", key_lengths=lens, plant=plant)
+    off = m - n
+    for b, ln in enumerate(lens):
+        for i in range(n):
+            if i + off < ln:
+                np.testing.assert_allclose(O[b, :, i], Oc[b, :, i], atol=1e-12)
+                np.testing.assert_allclose(L[b, :, i], Lc[b, :, i], atol=1e-12)
+            if i + off >= ln - 1:
+                np.testing.assert_allclose(O[b, :, i], Op[b, :, i], atol=1e-12)
+                np.testing.assert_allclose(L[b, :, i], Lp[b, :, i], atol=1e-12)
+    assert any(i + off >= ln for ln in lens for i in range(n))      # both regimes occur
+    assert any(i + off < ln - 1 for ln in lens for i in range(n))
+
+
 PINS = [pin_worked_example, pin_causal_3x3, pin_rows_sum_to_one, pin_equal_scores_mean,
         pin_causal_row0, pin_permutation, pin_masked_exactly_zero, pin_fill_minus_1e9,
-        pin_library_brute_force, pin_two_key_logistic]
+        pin_library_brute_force, pin_two_key_logistic, pin_causal_suffix,
+        pin_causal_and_padding]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -244,7 +293,7 @@ def test_pin(pin):
     pin(0)
 
 
-@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_planted_mistake_is_caught(plant):
     caught = []
     for pin in PINS:
@@ -263,6 +312,19 @@ def test_fully_masked_row_reading():
     O, L = oracle.attn_fwd(Q, K, V, "key_padding", key_lengths=[0, 5])
     assert np.all(O[0] == 0.0) and np.all(np.isneginf(L[0]))
     assert np.all(np.isfinite(O[1])) and np.all(np.isfinite(L[1]))
+
+
+def test_causal_rows_without_keys_reading():
+    """Causal with n > m: query row i sees keys j <= i - (n - m), so the first n - m rows
+    see none and get O = 0, LSE = -inf (the same reading as a zero key length)."""
+    Q, K, V = rnd((1, 2, 7, 4), 36), rnd((1, 2, 3, 4), 37), rnd((1, 2, 3, 4), 38)
+    O, L = oracle.attn_fwd(Q, K, V, "causal")
+    assert np.all(O[:, :, :4] == 0.0) and np.all(np.isneginf(L[:, :, :4]))
+    Ot, Lt = _torch_ref(Q[:, :, 4:], K, V, "causal", None, 0.5)
+    np.testing.assert_allclose(O[:, :, 4:], Ot, atol=1e-12)
+    np.testing.assert_allclose(L[:, :, 4:], Lt, atol=1e-12)
+    O, L = oracle.attn_fwd(Q[:, :, :3], K, V, "causal_key_padding", key_lengths=[0])
+    assert np.all(O == 0.0) and np.all(np.isneginf(L))
 
 
 def test_key_length_clamp():

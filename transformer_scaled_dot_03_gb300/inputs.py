@@ -26,7 +26,9 @@ import torch
 MASK_NONE = "none"
 MASK_CAUSAL = "causal"
 MASK_KEY_PADDING = "key_padding"
-MASK_KINDS = (MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING)
+MASK_CAUSAL_KEY_PADDING = "causal_key_padding"
+MASK_KINDS = (MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING)
+LENGTH_MASKS = (MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -51,7 +53,7 @@ class Workload:
     def flops(self) -> float:
         """Nominal forward FLOPs: two GEMMs of 2*n*m*d each, halved for causal."""
         f = 4.0 * self.B * self.H * self.n * self.m * self.d_k
-        return f / 2 if self.mask == MASK_CAUSAL else f
+        return f / 2 if self.mask in (MASK_CAUSAL, MASK_CAUSAL_KEY_PADDING) else f
 
     def io_bytes(self) -> int:
         """Algorithmic HBM bytes: Q, K, V read once (bf16); O (bf16) and LSE (fp32) written once."""
@@ -103,7 +105,7 @@ def make_inputs(B, H, n, m, d_k, d_v, mask=MASK_NONE, seed=0, *, value_scale=1.0
                 len_lo=None, len_hi=None, key_lengths=None, scale=None) -> Inputs:
     """Draw i.i.d. N(0,1)*value_scale Q, K, V (in that order), then key lengths.
 
-    For ``mask == "key_padding"`` the valid lengths are ``randint(len_lo, len_hi+1)``
+    For the key-padding masks the valid lengths are ``randint(len_lo, len_hi+1)``
     unless ``key_lengths`` is given explicitly (a list/tensor of B ints).
     ``scale`` defaults to ``1/sqrt(d_k)``.
     """
@@ -118,7 +120,7 @@ def make_inputs(B, H, n, m, d_k, d_v, mask=MASK_NONE, seed=0, *, value_scale=1.0
 
 
 def _lengths(g, B, m, mask, len_lo, len_hi, key_lengths):
-    if mask != MASK_KEY_PADDING:
+    if mask not in LENGTH_MASKS:
         return None
     if key_lengths is not None:
         return torch.as_tensor(key_lengths, dtype=torch.int32).reshape(B).clone()
