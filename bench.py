@@ -178,9 +178,7 @@ def run_ours(args):
 
     w, x = make_workload(args.workload)
     flops = w.flops()
-    eff_flops = flops
-    if w.mask == inputs.MASK_KEY_PADDING:
-        eff_flops = 4.0 * w.H * w.d_k * w.n * float(x.key_lengths.clamp(0, w.m).sum())
+    eff_flops = effective_flops(w, x)
     in_bytes = x.Q.numel() * 2 + x.K.numel() * 2 + x.V.numel() * 2
     out_bytes = w.B * w.H * w.n * (w.d_v * 2 + 4)
     copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_bytes)))
@@ -298,7 +296,7 @@ def run_ours(args):
             "data": "synthetic (seeded; bias-free Xavier projections of X~N(0,1))",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "m": w.m,
                        "d_k": w.d_k, "d_v": w.d_v, "mask": w.mask,
-                       "key_lengths": [w.len_lo, w.len_hi] if w.mask == "key_padding" else None,
+                       "key_lengths": [w.len_lo, w.len_hi] if w.mask in inputs.LENGTH_MASKS else None,
                        "global_batch": w.B * world, "parallelism": f"replicas{world}",
                        "l2": f"rotating {copies} input/output sets "
                              f"({copies * (in_bytes + out_bytes) / 2**20:.0f} MiB > 2x L2)",
@@ -325,6 +323,22 @@ def run_ours(args):
     return result
 
 
+def effective_flops(w, x):
+    """FLOPs of the (query, key) pairs the masks leave visible, counted exactly with
+    the drawn key lengths: 2*(d_k + d_v) per pair."""
+    i = torch.arange(w.n, dtype=torch.float64)
+    if w.mask in (inputs.MASK_CAUSAL, inputs.MASK_CAUSAL_KEY_PADDING):
+        per_row_cap = (i + (w.m - w.n) + 1).clamp(0, w.m)      # keys j <= i + m - n
+    else:
+        per_row_cap = torch.full((w.n,), float(w.m), dtype=torch.float64)
+    if x.key_lengths is not None:
+        lens = x.key_lengths.to(torch.float64).clamp(0, w.m)
+        pairs = float(torch.minimum(per_row_cap[None, :], lens[:, None]).sum()) * w.H
+    else:
+        pairs = float(per_row_cap.sum()) * w.B * w.H
+    return 2.0 * (w.d_k + w.d_v) * pairs
+
+
 def cpu_baseline(w, x, seconds):
     """The fp64 oracle as it stands, on all host cores, over a seeded sample of
     query rows of the same workload; scaled to TFLOP/s of the nominal FLOP model."""
@@ -332,7 +346,7 @@ def cpu_baseline(w, x, seconds):
 
     threads = oracle.default_threads()
     total_rows = w.B * w.H * w.n
-    per_row = 4.0 * w.m * w.d_k * (0.5 if w.mask == "causal" else 1.0)
+    per_row = w.flops() / (w.B * w.H * w.n)
     # calibrate on a small sample, then size the sample to about `seconds`
     probe = inputs.sample_rows(w.B, w.H, w.n, min(total_rows, 64 * threads), seed=11)
     t0 = time.perf_counter()
@@ -360,7 +374,7 @@ def run_reference(args):
     oracle.build()
     threads = oracle.default_threads()
     total_rows = w.B * w.H * w.n
-    per_row = 4.0 * w.m * w.d_k * (0.5 if w.mask == "causal" else 1.0)
+    per_row = w.flops() / (w.B * w.H * w.n)
     probe = inputs.sample_rows(w.B, w.H, w.n, min(total_rows, 16 * threads), seed=21)
     t0 = time.perf_counter()
     oracle.attn_rows(x.Q, x.K, x.V, probe, w.mask, x.key_lengths, x.scale, threads=threads)
@@ -399,7 +413,7 @@ def main():
     ap.add_argument("--steps", type=int, default=65536)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER + inputs.VARIANT_ORDER)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -12,11 +12,20 @@
  * where M_bij is 0 for a visible key and -inf for a masked one:
  *     ATTN_MASK_NONE         every key is visible (encoder self-attention,
  *                            cross-attention without padding);
- *     ATTN_MASK_CAUSAL       key j is visible to query i iff j <= i (decoder
- *                            self-attention, "Transformer 详解" §5.3);
+ *     ATTN_MASK_CAUSAL       key j is visible to query i iff j <= i + (m - n)
+ *                            (decoder self-attention, "Transformer 详解" §5.3,
+ *                            which prints the square case n = m; for n != m
+ *                            the n queries are the last n of the m positions,
+ *                            as when new queries attend to a cache of m keys,
+ *                            so with n > m the first n - m rows see no key);
  *     ATTN_MASK_KEY_PADDING  key j is visible iff j < key_lengths[b], for all
  *                            query rows (the [batch,1,1,seq] pad mask of
- *                            "Transformer 详解" §3.4 for tail-padded batches).
+ *                            "Transformer 详解" §3.4 for tail-padded batches);
+ *     ATTN_MASK_CAUSAL_KEY_PADDING
+ *                            both conditions at once (the decoder target mask
+ *                            of "Transformer 详解" §5.3: pad mask AND
+ *                            subsequent mask).
+ * A row that sees no key gets O = 0 and LSE = -inf.
  * The n x m score matrix is never written to memory. LSE is the per-row
  * natural-log normaliser (not printed on the pages; a standard by-product
  * needed to merge or differentiate attention).
@@ -48,15 +57,16 @@ extern "C" {
 typedef enum {
     ATTN_MASK_NONE = 0,
     ATTN_MASK_CAUSAL = 1,
-    ATTN_MASK_KEY_PADDING = 2
+    ATTN_MASK_KEY_PADDING = 2,
+    ATTN_MASK_CAUSAL_KEY_PADDING = 3
 } attn_mask_kind_t;
 
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad mask kind,
-                                  causal with n != m, KEY_PADDING without lengths */
-    ATTN_ERR_UNSUPPORTED = -2, /* head dims other than d_k = d_v in {64, 128}, or
-                                  sizes beyond the kernel's index range */
+                                  a key-padding mask without lengths */
+    ATTN_ERR_UNSUPPORTED = -2, /* a head dim outside {64, 128}, n or m above
+                                  2^30, or B*H*ceil(n/128) beyond int range */
     ATTN_ERR_MISALIGNED = -3,  /* Q, K, V or O not 16-byte aligned; LSE or
                                   key_lengths not 4-byte aligned */
     ATTN_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (message in
@@ -68,10 +78,10 @@ typedef enum {
  * Attention forward. See the file comment for the operation and layouts.
  *   B, H, n, m   batch, heads, query rows, key/value rows. B, H or n equal to 0
  *                is a no-op; m = 0 writes O = 0 and LSE = -inf.
- *   d_k, d_v     head dims; supported: d_k == d_v in {64, 128}.
- *   mask_kind    attn_mask_kind_t. CAUSAL requires n == m (the pages define the
- *                square mask only).
- *   key_lengths  device int32 [B]; required for KEY_PADDING, ignored otherwise.
+ *   d_k, d_v     head dims, each 64 or 128 (d_k != d_v allowed).
+ *   mask_kind    attn_mask_kind_t.
+ *   key_lengths  device int32 [B]; required for KEY_PADDING and
+ *                CAUSAL_KEY_PADDING, ignored otherwise.
  *                Values are read on the device and clamped to [0, m]; a length
  *                of 0 gives O = 0 and LSE = -inf for every row of that entry.
  *   scale        multiplies q.k; a value <= 0, NaN or inf selects 1/sqrt(d_k)

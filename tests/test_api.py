@@ -57,13 +57,16 @@ def call(Q=P, K=P, V=P, B=1, H=1, n=4, m=4, dk=64, dv=64, mask=0, lens=None, O=P
     (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
     (dict(n=-3), attn.ATTN_ERR_INVALID_ARG),
     (dict(m=-1), attn.ATTN_ERR_INVALID_ARG),
-    (dict(mask=3), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=4), attn.ATTN_ERR_INVALID_ARG),
     (dict(mask=-1), attn.ATTN_ERR_INVALID_ARG),
-    (dict(mask=1, n=4, m=5), attn.ATTN_ERR_INVALID_ARG),          # causal needs n == m
     (dict(mask=2, lens=None), attn.ATTN_ERR_INVALID_ARG),         # key padding needs lengths
+    (dict(mask=3, lens=None), attn.ATTN_ERR_INVALID_ARG),
     (dict(dk=32, dv=32), attn.ATTN_ERR_UNSUPPORTED),
-    (dict(dk=64, dv=128), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dk=64, dv=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dk=256, dv=128), attn.ATTN_ERR_UNSUPPORTED),
     (dict(dk=96, dv=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(n=(1 << 30) + 1), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(m=(1 << 30) + 1, mask=1), attn.ATTN_ERR_UNSUPPORTED),
     (dict(Q=None), attn.ATTN_ERR_INVALID_ARG),
     (dict(O=None), attn.ATTN_ERR_INVALID_ARG),
     (dict(Q=ctypes.c_void_p(0x10008)), attn.ATTN_ERR_MISALIGNED),
@@ -92,3 +95,11 @@ def test_binding_fails_loudly_without_gpu_tensors(lib):
 def test_flop_model():
     assert attn.flops(32, 8, 512, 512, 64, "key_padding") == 4.0 * 32 * 8 * 512 * 512 * 64
     assert attn.flops(16, 16, 1024, 1024, 64, "causal") == 2.0 * 16 * 16 * 1024 * 1024 * 64
+    assert attn.flops(1, 1, 1024, 1024, 64, "causal_key_padding") == attn.flops(1, 1, 1024, 1024, 64,
+                                                                                "causal")
+    # one query against m keys sees them all (within half a pair of the exact count)
+    assert abs(attn.flops(1, 1, 1, 4096, 64, "causal") - 4.0 * 64 * 4096) <= 4.0 * 64 * 0.5
+    # the masked triangle's nominal area shrinks as n falls below m
+    assert attn.flops(1, 1, 256, 1024, 64, "causal") == 4.0 * 64 * (256 * 1024 - 256 * 256 / 2)
+    assert attn.flops(1, 1, 1024, 256, 64, "causal") == 4.0 * 64 * 256 * 256 / 2
+    assert attn.flops(2, 3, 128, 96, 64, "none", d_v=128) == 2.0 * 2 * 3 * (64 + 128) * 128 * 96

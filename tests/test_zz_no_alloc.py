@@ -45,7 +45,7 @@ def call_noalloc(lib, Q, K, V, mask, lens, scale, O, L):
 
 
 @pytest.mark.parametrize("mask,d,n,m", [("key_padding", 64, 300, 300), ("causal", 128, 200, 200),
-                                        ("none", 64, 100, 513)])
+                                        ("none", 64, 100, 513), ("causal_key_padding", 64, 150, 400)])
 def test_noalloc_matches_attn_fwd(lib, mask, d, n, m):
     x = inputs.make_inputs(2, 3, n, m, d, d, mask, seed=9100 + d + n, len_lo=1, len_hi=m)
     Q, K, V = x.Q.cuda(), x.K.cuda(), x.V.cuda()
@@ -83,7 +83,8 @@ def test_noalloc_rejects_bad_arguments(lib):
     L = torch.zeros(1, 1, 4, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     rc = lib.attn_fwd_noalloc(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(q.data_ptr()),
-                              ctypes.c_void_p(q.data_ptr()), 1, 1, 4, 5, 64, 64, attn.MASK_CODES["causal"],
+                              ctypes.c_void_p(q.data_ptr()), 1, 1, 4, 4, 64, 64,
+                              attn.MASK_CODES["causal_key_padding"],
                               None, ctypes.c_float(-1.0), ctypes.c_void_p(O.data_ptr()),
                               ctypes.c_void_p(L.data_ptr()), ctypes.c_void_p(stream))
     assert rc == attn.ATTN_ERR_INVALID_ARG

@@ -28,7 +28,8 @@ ATTN_ERR_MISALIGNED = -3
 ATTN_ERR_CUDA = -4
 ATTN_ERR_TIMEOUT = -5
 
-MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PADDING: 2}
+MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PADDING: 2,
+              _inputs.MASK_CAUSAL_KEY_PADDING: 3}
 
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
@@ -99,10 +100,10 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "non
              key_lengths: torch.Tensor | None = None, scale: float | None = None,
              O: torch.Tensor | None = None, LSE: torch.Tensor | None = None,
              want_lse: bool = True, stream=None):
-    """Attention forward on the GPU. Q [B,H,n,d], K [B,H,m,d], V [B,H,m,d] bf16 CUDA
-    tensors (contiguous); ``key_lengths`` int32 CUDA [B] for ``mask="key_padding"``.
-    Returns (O [B,H,n,d] bf16, LSE [B,H,n] fp32 or None). Asynchronous on ``stream``
-    (default: PyTorch's current stream)."""
+    """Attention forward on the GPU. Q [B,H,n,d_k], K [B,H,m,d_k], V [B,H,m,d_v] bf16
+    CUDA tensors (contiguous); ``key_lengths`` int32 CUDA [B] for the key-padding masks
+    ("key_padding", "causal_key_padding"). Returns (O [B,H,n,d_v] bf16, LSE [B,H,n] fp32
+    or None). Asynchronous on ``stream`` (default: PyTorch's current stream)."""
     if mask not in MASK_CODES:
         raise ValueError(f"unknown mask {mask!r}")
     for name, t in (("Q", Q), ("K", K), ("V", V)):
@@ -113,17 +114,18 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "non
     d_v = V.shape[3]
     if tuple(K.shape) != (B, H, m, d_k) or tuple(V.shape[:3]) != (B, H, m):
         raise ValueError("inconsistent Q/K/V shapes")
-    if mask == "key_padding":
+    uses_lengths = mask in _inputs.LENGTH_MASKS
+    if uses_lengths:
         if key_lengths is None or key_lengths.dtype != torch.int32 or not key_lengths.is_cuda \
                 or key_lengths.numel() != B or not key_lengths.is_contiguous():
-            raise ValueError("key_padding needs key_lengths: contiguous int32 CUDA [B]")
+            raise ValueError(f"{mask} needs key_lengths: contiguous int32 CUDA [B]")
     if O is None:
         O = torch.empty((B, H, n, d_v), dtype=torch.bfloat16, device=Q.device)
     if LSE is None and want_lse:
         LSE = torch.empty((B, H, n), dtype=torch.float32, device=Q.device)
     sc = -1.0 if scale is None else float(scale)
     rc = attn_fwd_raw(_ptr(Q), _ptr(K), _ptr(V), B, H, n, m, d_k, d_v, MASK_CODES[mask],
-                      _ptr(key_lengths) if mask == "key_padding" else None, sc, _ptr(O), _ptr(LSE),
+                      _ptr(key_lengths) if uses_lengths else None, sc, _ptr(O), _ptr(LSE),
                       _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd", last_error() if rc == ATTN_ERR_CUDA else "")
@@ -141,10 +143,13 @@ def set_watchdog(limit_ns: int = 0, debug_flags: int = 0) -> None:
     load().attn_set_watchdog(ctypes.c_uint64(limit_ns), ctypes.c_uint32(debug_flags))
 
 
-def flops(B, H, n, m, d_k, mask) -> float:
-    """Nominal forward FLOPs: 4*B*H*n*m*d_k, halved for causal."""
-    f = 4.0 * B * H * n * m * d_k
-    return f / 2 if mask == "causal" else f
+def flops(B, H, n, m, d_k, mask, d_v=None) -> float:
+    """Nominal forward FLOPs: 2*B*H*(d_k + d_v) per visible (query, key) pair (d_v
+    defaults to d_k). Without a causal mask every pair counts (n*m); with it the masked
+    triangle counts as half its square, n*m - n*n/2 for n <= m (n*m/2 when n = m) and
+    m*m/2 for n > m."""
+    d_v = d_k if d_v is None else d_v
+    return 2.0 * B * H * (d_k + d_v) * _inputs.nominal_pairs(n, m, mask)
 
 
 def default_scale(d_k: int) -> float:

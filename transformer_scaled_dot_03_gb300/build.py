@@ -1,6 +1,6 @@
 """Build ``libattn_sm103a.so`` (the C-ABI attention library) in-tree with nvcc.
 
-One ``-gencode arch=compute_103a,code=sm_103a`` target; the three translation
+One ``-gencode arch=compute_103a,code=sm_103a`` target; the translation
 units compile in parallel, then link into a shared library next to this file.
 The CUDA runtime is linked statically, so the library does not depend on the
 runtime version that PyTorch ships.
@@ -18,7 +18,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_sm103a.so")
-SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu", "attn_fwd_dmix.cu"]
 HEADERS = ["attn_internal.h", "attn_kernel.cuh", "attn_kernel_dp.cuh", "sm103a.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

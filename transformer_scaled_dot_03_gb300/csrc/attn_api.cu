@@ -20,6 +20,7 @@ namespace {
 
 constexpr uint64_t kDefaultWatchdogNs = 2000000000ull;   // 2 s per device-side wait
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSeq = 1 << 30;   // n, m: row indices plus a tile stay within int
 
 std::mutex g_mu;
 uint32_t* g_status[kMaxDevices] = {};
@@ -128,10 +129,11 @@ int sm_count(int* out)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Kernel variant per head dim. Defaults: one tile per CTA with P apart from S
-// (KERNEL_DP) at both d = 64 and d = 128. ATTN_KERNEL=dp|nt1|nt2 overrides it
-// (a tuning knob for measurements, read once).
-int kernel_variant(int d)
+// Kernel variant. Default: the persistent kernel with P apart from S
+// (KERNEL_DP). ATTN_KERNEL=dp|nt1|nt2 overrides it (a tuning knob for
+// measurements, read once); the NT variants only take d_k = d_v and the masks
+// none, causal with n = m, and key padding, so other calls keep KERNEL_DP.
+int kernel_variant(int d_k, int d_v, int mask_kind, int n, int m)
 {
     static int env = [] {
         const char* v = std::getenv("ATTN_KERNEL");
@@ -141,9 +143,97 @@ int kernel_variant(int d)
         if (std::strcmp(v, "nt2") == 0) return static_cast<int>(attn::KERNEL_NT2);
         return -1;
     }();
-    if (env >= 0) return env;
-    (void)d;
-    return attn::KERNEL_DP;
+    const bool nt_ok = d_k == d_v && mask_kind != ATTN_MASK_CAUSAL_KEY_PADDING &&
+                       !(mask_kind == ATTN_MASK_CAUSAL && n != m);
+    return (env >= 0 && nt_ok) ? env : static_cast<int>(attn::KERNEL_DP);
+}
+
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+
+// Host-side checks shared by both entry points.
+int validate(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k, int d_v,
+             int mask_kind, const int32_t* key_lengths, void* O, float* LSE)
+{
+    if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
+    if (attn::mask_has_lengths(mask_kind) && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_ok(d_k) || !head_dim_ok(d_v)) return ATTN_ERR_UNSUPPORTED;
+    if (n > kMaxSeq || m > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || n == 0) return ATTN_OK;   // nothing to compute
+    if (O == nullptr || (m > 0 && (Q == nullptr || K == nullptr || V == nullptr)))
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(O, 16) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16))
+        return ATTN_ERR_MISALIGNED;
+    if ((LSE != nullptr && !aligned(LSE, 4)) || (key_lengths != nullptr && !aligned(key_lengths, 4)))
+        return ATTN_ERR_MISALIGNED;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    const int64_t num_qblocks = (static_cast<int64_t>(n) + 255) / 128;   // worst case over the variants
+    if (bh > INT32_MAX || bh * num_qblocks > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+// m = 0: no keys at all, every row gets O = 0 and LSE = -inf.
+int fill_no_keys(int64_t bh, int n, int d_v, void* O, float* LSE, cudaStream_t st)
+{
+    const int64_t rows = bh * n;
+    const int64_t elems = rows * d_v;
+    const int64_t blocks = std::min<int64_t>((elems + 255) / 256, 152 * 8);
+    fill_no_keys_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint16_t*>(O), elems, LSE,
+                                                                       rows);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : fail_cuda("fill kernel launch", e);
+}
+
+// Tensor maps, parameters and the launch of the attention kernel (m >= 1),
+// with `status` as the kernel's device status word.
+int launch_attention(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+                     int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
+                     uint32_t* status, cudaStream_t st)
+{
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    const int variant = kernel_variant(d_k, d_v, mask_kind, n, m);
+    const int64_t rows_per_cta = attn::kernel_rows_per_cta(variant);
+    const int64_t num_qblocks = (static_cast<int64_t>(n) + rows_per_cta - 1) / rows_per_cta;
+
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    int rc = encoder(&enc);
+    if (rc != ATTN_OK) return rc;
+    attn::TensorMaps maps;
+    if ((rc = make_map(enc, &maps.q, Q, bh, n, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.k, K, bh, m, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.v, V, bh, m, d_v, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.o, O, bh, n, d_v, 32)) != ATTN_OK) return rc;
+
+    const double sc = (scale > 0.f && std::isfinite(scale)) ? static_cast<double>(scale)
+                                                             : 1.0 / std::sqrt(static_cast<double>(d_k));
+    const bool paired = variant == attn::KERNEL_DP && attn::mask_is_causal(mask_kind);
+    attn::FwdParams p;
+    p.B = B;
+    p.H = H;
+    p.n = n;
+    p.m = m;
+    p.causal_off = m - n;
+    p.num_qblocks = static_cast<int>(num_qblocks);
+    p.num_units = static_cast<int>(bh * (paired ? (num_qblocks + 1) / 2 : num_qblocks));
+    p.O = O;
+    p.key_lengths = attn::mask_has_lengths(mask_kind) ? key_lengths : nullptr;
+    p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
+    p.LSE = LSE;
+    p.status = status;
+    p.watchdog_ns = g_watchdog_ns;
+    p.debug_flags = g_debug_flags;
+
+    int num_sms = 0;
+    if ((rc = sm_count(&num_sms)) != ATTN_OK) return rc;
+    const int64_t ctas = bh * num_qblocks;
+    cudaError_t e;
+    if (d_k != d_v)
+        e = attn::launch_fwd_dmix(d_k, d_v, mask_kind, maps, p, num_sms, st);
+    else if (d_k == 64)
+        e = attn::launch_fwd_d64(mask_kind, variant, maps, p, ctas, num_sms, st);
+    else
+        e = attn::launch_fwd_d128(mask_kind, variant, maps, p, ctas, num_sms, st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda("attention kernel launch", e);
 }
 
 }  // namespace
@@ -154,73 +244,13 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
              int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
              void* stream)
 {
-    if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
-    if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
-    if (mask_kind == ATTN_MASK_CAUSAL && n != m) return ATTN_ERR_INVALID_ARG;
-    if (mask_kind == ATTN_MASK_KEY_PADDING && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
-    if (!(d_k == d_v && (d_k == 64 || d_k == 128))) return ATTN_ERR_UNSUPPORTED;
-    if (B == 0 || H == 0 || n == 0) return ATTN_OK;   // nothing to compute
-    if (O == nullptr || (m > 0 && (Q == nullptr || K == nullptr || V == nullptr)))
-        return ATTN_ERR_INVALID_ARG;
-    if (!aligned(O, 16) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16))
-        return ATTN_ERR_MISALIGNED;
-    if ((LSE != nullptr && !aligned(LSE, 4)) || (key_lengths != nullptr && !aligned(key_lengths, 4)))
-        return ATTN_ERR_MISALIGNED;
-
-    const int64_t bh = static_cast<int64_t>(B) * H;
-    const int variant = kernel_variant(d_k);
-    const int64_t rows_per_cta = attn::kernel_rows_per_cta(variant);
-    const int64_t num_qblocks = (static_cast<int64_t>(n) + rows_per_cta - 1) / rows_per_cta;
-    if (bh > INT32_MAX || bh * num_qblocks > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    int rc = validate(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, O, LSE);
+    if (rc != ATTN_OK || B == 0 || H == 0 || n == 0) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-    if (m == 0) {
-        const int64_t rows = bh * n;
-        const int64_t elems = rows * d_v;
-        const int64_t blocks = std::min<int64_t>((elems + 255) / 256, 152 * 8);
-        fill_no_keys_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-            static_cast<uint16_t*>(O), elems, LSE, rows);
-        cudaError_t e = cudaGetLastError();
-        return e == cudaSuccess ? ATTN_OK : fail_cuda("fill kernel launch", e);
-    }
-
+    if (m == 0) return fill_no_keys(static_cast<int64_t>(B) * H, n, d_v, O, LSE, st);
     uint32_t* status = nullptr;
-    int rc = status_word(&status);
-    if (rc != ATTN_OK) return rc;
-    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    rc = encoder(&enc);
-    if (rc != ATTN_OK) return rc;
-
-    attn::TensorMaps maps;
-    if ((rc = make_map(enc, &maps.q, Q, bh, n, d_k, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(enc, &maps.k, K, bh, m, d_k, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(enc, &maps.v, V, bh, m, d_v, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(enc, &maps.o, O, bh, n, d_v, 32)) != ATTN_OK) return rc;
-
-    const double sc = (scale > 0.f && std::isfinite(scale)) ? static_cast<double>(scale)
-                                                             : 1.0 / std::sqrt(static_cast<double>(d_k));
-    attn::FwdParams p;
-    p.B = B;
-    p.H = H;
-    p.n = n;
-    p.m = m;
-    p.num_qblocks = static_cast<int>(num_qblocks);
-    p.num_units = static_cast<int>(
-        bh * (variant == attn::KERNEL_DP && mask_kind == ATTN_MASK_CAUSAL ? (num_qblocks + 1) / 2 : num_qblocks));
-    p.O = O;
-    p.key_lengths = mask_kind == ATTN_MASK_KEY_PADDING ? key_lengths : nullptr;
-    p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
-    p.LSE = LSE;
-    p.status = status;
-    p.watchdog_ns = g_watchdog_ns;
-    p.debug_flags = g_debug_flags;
-
-    int num_sms = 0;
-    if ((rc = sm_count(&num_sms)) != ATTN_OK) return rc;
-    const int64_t ctas = bh * num_qblocks;
-    cudaError_t e = d_k == 64 ? attn::launch_fwd_d64(mask_kind, variant, maps, p, ctas, num_sms, st)
-                              : attn::launch_fwd_d128(mask_kind, variant, maps, p, ctas, num_sms, st);
-    return e == cudaSuccess ? ATTN_OK : fail_cuda("attention kernel launch", e);
+    if ((rc = status_word(&status)) != ATTN_OK) return rc;
+    return launch_attention(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, scale, O, LSE, status, st);
 }
 
 int attn_get_device_status(void* stream, uint32_t* detail)
@@ -312,22 +342,8 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int
                                 int d_k, int d_v, int mask_kind, const int32_t* key_lengths, float scale,
                                 void* O, float* LSE, void* stream)
 {
-    if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
-    if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
-    if (mask_kind == ATTN_MASK_CAUSAL && n != m) return ATTN_ERR_INVALID_ARG;
-    if (mask_kind == ATTN_MASK_KEY_PADDING && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
-    if (!(d_k == d_v && (d_k == 64 || d_k == 128))) return ATTN_ERR_UNSUPPORTED;
-    if (B == 0 || H == 0 || n == 0) return ATTN_OK;
-    if (O == nullptr || (m > 0 && (Q == nullptr || K == nullptr || V == nullptr))) return ATTN_ERR_INVALID_ARG;
-    if (!aligned(O, 16) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return ATTN_ERR_MISALIGNED;
-    if ((LSE != nullptr && !aligned(LSE, 4)) || (key_lengths != nullptr && !aligned(key_lengths, 4)))
-        return ATTN_ERR_MISALIGNED;
-
-    const int64_t bh = static_cast<int64_t>(B) * H;
-    const int variant = kernel_variant(d_k);
-    const int64_t rows_per_cta = attn::kernel_rows_per_cta(variant);
-    const int64_t num_qblocks = (static_cast<int64_t>(n) + rows_per_cta - 1) / rows_per_cta;
-    if (bh > INT32_MAX || bh * num_qblocks > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    int rc = validate(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, O, LSE);
+    if (rc != ATTN_OK || B == 0 || H == 0 || n == 0) return rc;
     // The kernel's scratch for one call is the status word, whatever the sizes;
     // anything larger than the array would be refused here.
     if (kNoAllocStatusBytes > kNoAllocScratchBytes) {
@@ -336,54 +352,12 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int
         return ATTN_ERR_UNSUPPORTED;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-    if (m == 0) {
-        const int64_t rows = bh * n;
-        const int64_t elems = rows * d_v;
-        const int64_t blocks = std::min<int64_t>((elems + 255) / 256, 152 * 8);
-        fill_no_keys_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint16_t*>(O), elems,
-                                                                           LSE, rows);
-        cudaError_t e = cudaGetLastError();
-        return e == cudaSuccess ? ATTN_OK : fail_cuda("fill kernel launch", e);
-    }
+    if (m == 0) return fill_no_keys(static_cast<int64_t>(B) * H, n, d_v, O, LSE, st);
 
     uint32_t* scratch = nullptr;
-    int rc = noalloc_scratch(&scratch);
-    if (rc != ATTN_OK) return rc;
+    if ((rc = noalloc_scratch(&scratch)) != ATTN_OK) return rc;
     // the status word must start at zero; it keeps the previous call's value otherwise
     cudaError_t e = cudaMemsetAsync(scratch, 0, kNoAllocStatusBytes, st);
     if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(no-allocation scratch)", e);
-    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    if ((rc = encoder(&enc)) != ATTN_OK) return rc;
-
-    attn::TensorMaps maps;
-    if ((rc = make_map(enc, &maps.q, Q, bh, n, d_k, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(enc, &maps.k, K, bh, m, d_k, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(enc, &maps.v, V, bh, m, d_v, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(enc, &maps.o, O, bh, n, d_v, 32)) != ATTN_OK) return rc;
-
-    const double sc = (scale > 0.f && std::isfinite(scale)) ? static_cast<double>(scale)
-                                                             : 1.0 / std::sqrt(static_cast<double>(d_k));
-    attn::FwdParams p;
-    p.B = B;
-    p.H = H;
-    p.n = n;
-    p.m = m;
-    p.num_qblocks = static_cast<int>(num_qblocks);
-    p.num_units = static_cast<int>(
-        bh * (variant == attn::KERNEL_DP && mask_kind == ATTN_MASK_CAUSAL ? (num_qblocks + 1) / 2 : num_qblocks));
-    p.O = O;
-    p.key_lengths = mask_kind == ATTN_MASK_KEY_PADDING ? key_lengths : nullptr;
-    p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
-    p.LSE = LSE;
-    p.status = scratch;
-    p.watchdog_ns = g_watchdog_ns;
-    p.debug_flags = g_debug_flags;
-
-    int num_sms = 0;
-    if ((rc = sm_count(&num_sms)) != ATTN_OK) return rc;
-    const int64_t ctas = bh * num_qblocks;
-    e = d_k == 64 ? attn::launch_fwd_d64(mask_kind, variant, maps, p, ctas, num_sms, st)
-                  : attn::launch_fwd_d128(mask_kind, variant, maps, p, ctas, num_sms, st);
-    return e == cudaSuccess ? ATTN_OK : fail_cuda("attention kernel launch", e);
+    return launch_attention(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, scale, O, LSE, scratch, st);
 }

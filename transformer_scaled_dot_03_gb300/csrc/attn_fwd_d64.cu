@@ -20,9 +20,11 @@ static cudaError_t launch_dp(int mask, const TensorMaps& maps, const FwdParams& 
                              cudaStream_t stream)
 {
     switch (mask) {
-    case MASK_NONE: return dp::launch<64, MASK_NONE>(maps, p, num_sms, stream);
-    case MASK_CAUSAL: return dp::launch<64, MASK_CAUSAL>(maps, p, num_sms, stream);
-    case MASK_KEY_PADDING: return dp::launch<64, MASK_KEY_PADDING>(maps, p, num_sms, stream);
+    case MASK_NONE: return dp::launch<64, 64, MASK_NONE>(maps, p, num_sms, stream);
+    case MASK_CAUSAL: return dp::launch<64, 64, MASK_CAUSAL>(maps, p, num_sms, stream);
+    case MASK_KEY_PADDING: return dp::launch<64, 64, MASK_KEY_PADDING>(maps, p, num_sms, stream);
+    case MASK_CAUSAL_KEY_PADDING:
+        return dp::launch<64, 64, MASK_CAUSAL_KEY_PADDING>(maps, p, num_sms, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -8,7 +8,16 @@
 
 namespace attn {
 
-enum { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_KEY_PADDING = 2 };
+enum { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_KEY_PADDING = 2, MASK_CAUSAL_KEY_PADDING = 3 };
+
+__host__ __device__ constexpr bool mask_is_causal(int mask)
+{
+    return mask == MASK_CAUSAL || mask == MASK_CAUSAL_KEY_PADDING;
+}
+__host__ __device__ constexpr bool mask_has_lengths(int mask)
+{
+    return mask == MASK_KEY_PADDING || mask == MASK_CAUSAL_KEY_PADDING;
+}
 
 // Bits of the device status word: which bounded wait gave up.
 enum : uint32_t {
@@ -22,10 +31,11 @@ enum : uint32_t { DEBUG_FORCE_TIMEOUT = 1u };
 
 struct FwdParams {
     int B, H, n, m;
+    int causal_off;               // m - n: query row i sees keys j <= i + causal_off (causal masks)
     int num_qblocks;              // ceil(n / rows per work unit)
     int num_units;                // B * H * num_qblocks (persistent kernel)
     void* O;                      // bf16 [B,H,n,d_v] (persistent kernel stores rows directly)
-    const int32_t* key_lengths;   // device int32 [B] (key padding only)
+    const int32_t* key_lengths;   // device int32 [B] (key-padding masks only)
     float scale_log2;             // scale * log2(e)
     float* LSE;                   // fp32 [B,H,n] or null
     uint32_t* status;             // device status word
@@ -46,9 +56,13 @@ enum { KERNEL_DP = 0, KERNEL_NT1 = 1, KERNEL_NT2 = 2 };
 inline int kernel_rows_per_cta(int variant) { return variant == KERNEL_NT2 ? 256 : 128; }
 
 // num_ctas: grid of the one-unit-per-CTA variants; num_sms sizes the persistent grid.
+// The NT variants take d_k = d_v, masks none / causal (n = m) / key padding.
 cudaError_t launch_fwd_d64(int mask, int variant, const TensorMaps& maps, const FwdParams& p,
                            int64_t num_ctas, int num_sms, cudaStream_t stream);
 cudaError_t launch_fwd_d128(int mask, int variant, const TensorMaps& maps, const FwdParams& p,
                             int64_t num_ctas, int num_sms, cudaStream_t stream);
+// d_k != d_v (64 and 128 either way round), persistent kernel only.
+cudaError_t launch_fwd_dmix(int d_k, int d_v, int mask, const TensorMaps& maps, const FwdParams& p,
+                            int num_sms, cudaStream_t stream);
 
 }  // namespace attn

@@ -2,9 +2,10 @@
 // tiles, P held apart from S in tensor memory ("decoupled P").
 //
 // Computes the scaled dot-product attention of "Transformer 详解" §4.1-§4.2
-// (scores = Q Kᵀ / sqrt(d_k), the causal mask of §5.3 or the key-padding mask
-// of §3.4, row softmax, weights x V) with an online softmax over 128-key tiles,
-// per (batch, head) pair.
+// (scores = Q Kᵀ / sqrt(d_k), the causal mask of §5.3, the key-padding mask of
+// §3.4 or both at once, row softmax, weights x V) with an online softmax over
+// 128-key tiles, per (batch, head) pair. Under the causal mask query row i sees
+// keys j <= i + (m - n): the n queries are the last n of the m positions.
 //
 // Schedule. A work unit is one (b, h) pair and one 128-row query tile (two
 // tiles, longest with shortest, under the causal mask); each CTA takes units
@@ -22,10 +23,10 @@
 //   warp  4     TMA producer: Q, then a K ring and a V ring (K runs one tile ahead)
 //   warp  5     tcgen05.mma issuer, owns the TMEM allocation
 //   warps 6-7   idle (complete the control warpgroup for setmaxnreg)
-// Tensor memory: S [0,128), P [128,192), O [192,192+D), at d = 128 also two Q
-// buffers [320,384), [384,448).
-//   d = 64 : 256 columns, 96 KB shared memory -> two CTAs per SM
-//   d = 128: 512 columns, 224 KB shared memory -> one CTA per SM
+// Tensor memory: S [0,128), P [128,192), O [192,192+d_v), at d_k = 128 also two
+// Q buffers of 64 columns after O.
+//   d_k = d_v = 64: 256 columns, 96 KB shared memory -> two CTAs per SM
+//   otherwise     : 512 columns, up to 224 KB shared memory -> one CTA per SM
 // O leaves through a shared-memory staging tile and per-warp TMA stores that
 // are only waited for before the staging tile is reused.
 #pragma once
@@ -52,22 +53,27 @@ constexpr float LN2 = 0.693147180559945309f;
 // sums hold as well as values <= 1, and O needs no rescaling.
 constexpr float RESCALE_LOG2 = 8.0f;
 
-template <int D>
+// Q and K tiles are 128 x d_k, V and O tiles 128 x d_v, each stored as 64-column
+// chunks of 16 KB (128-byte rows, 128-byte swizzle).
+template <int DK, int DV>
 struct Layout {
-    static constexpr int CH = D / 64;
-    static constexpr int TILE = CH * CHUNK_BYTES;
+    static constexpr int CHK = DK / 64;
+    static constexpr int CHV = DV / 64;
+    static constexpr int TILE_K = CHK * CHUNK_BYTES;   // a Q or K tile
+    static constexpr int TILE_V = CHV * CHUNK_BYTES;   // a V or O tile
     static constexpr int NUM_THREADS = 256;
     static constexpr int WARP_TMA = 4;
     static constexpr int WARP_MMA = 5;
-    static constexpr int CTAS_PER_SM = D == 64 ? 2 : 1;
-    static constexpr bool Q_IN_TMEM = D == 128;
-    static constexpr int KS = D == 64 ? 2 : 3;         // K ring depth
+    static constexpr bool SMALL = DK == 64 && DV == 64;
+    static constexpr int CTAS_PER_SM = SMALL ? 2 : 1;
+    static constexpr bool Q_IN_TMEM = DK == 128;
+    static constexpr int KS = SMALL ? 2 : 3;           // K ring depth
     static constexpr int VS = 2;                       // V ring depth
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + TILE;
-    static constexpr int V_OFF = K_OFF + KS * TILE;
-    static constexpr int OST_OFF = V_OFF + VS * TILE;  // O staging tile
-    static constexpr int BAR_OFF = OST_OFF + TILE;
+    static constexpr int K_OFF = Q_OFF + TILE_K;
+    static constexpr int V_OFF = K_OFF + KS * TILE_K;
+    static constexpr int OST_OFF = V_OFF + VS * TILE_V;  // O staging tile
+    static constexpr int BAR_OFF = OST_OFF + TILE_V;
     static constexpr int B_QFULL = 0;               // Q of a tile loaded               (tx)
     static constexpr int B_QFREE = 1;               // Q buffer may be refilled
     static constexpr int B_QREADY = 2;              // Q copied into tensor memory      (128 arrivals)
@@ -84,14 +90,14 @@ struct Layout {
     static constexpr int NBARS = B_NEVER + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16 + 1024;
-    static constexpr uint32_t TMEM_COLS = D == 64 ? 256 : 512;
-    static constexpr uint32_t S_COL = 0, P_COL = 128, O_COL = 192, QT_COL = 192 + D;
+    static constexpr uint32_t TMEM_COLS = SMALL ? 256 : 512;
+    static constexpr uint32_t S_COL = 0, P_COL = 128, O_COL = 192, QT_COL = 192 + DV;
     static constexpr uint32_t REG_LAUNCH = (65536 / (NUM_THREADS * CTAS_PER_SM)) / 8 * 8;
     static constexpr uint32_t REG_CTRL = 72;
     static constexpr uint32_t REG_SOFTMAX_FIT = ((REG_LAUNCH * NUM_THREADS - REG_CTRL * 128) / 128) / 8 * 8;
     static constexpr uint32_t REG_SOFTMAX = REG_SOFTMAX_FIT > 248 ? 248 : REG_SOFTMAX_FIT;
     static_assert(128 * REG_SOFTMAX + 128 * REG_CTRL <= REG_LAUNCH * NUM_THREADS, "register split");
-    static_assert((Q_IN_TMEM ? QT_COL + D : O_COL + D) <= TMEM_COLS, "tensor memory layout");
+    static_assert((Q_IN_TMEM ? QT_COL + DK : O_COL + DV) <= TMEM_COLS, "tensor memory layout");
     static_assert(BYTES <= (CTAS_PER_SM == 2 ? 115712 : 232448), "shared memory budget");
 };
 
@@ -116,13 +122,13 @@ struct Unit {
 // plain round-robin over units balances the CTAs.
 __host__ __device__ inline int units_per_head(int num_qblocks, int mask)
 {
-    return mask == MASK_CAUSAL ? (num_qblocks + 1) / 2 : num_qblocks;
+    return mask_is_causal(mask) ? (num_qblocks + 1) / 2 : num_qblocks;
 }
 
 template <int MASK>
 __device__ __forceinline__ int tiles_of_unit(int u, const FwdParams& p)
 {
-    if (MASK != MASK_CAUSAL) return 1;
+    if (!mask_is_causal(MASK)) return 1;
     const int k = u % units_per_head(p.num_qblocks, MASK);
     return (k == p.num_qblocks - 1 - k) ? 1 : 2;
 }
@@ -134,18 +140,18 @@ __device__ __forceinline__ Unit tile_of(int u, int i, const FwdParams& p)
     const int uph = units_per_head(p.num_qblocks, MASK);
     w.bh = u / uph;
     const int k = u % uph;
-    const int qb = (MASK == MASK_CAUSAL) ? (i == 0 ? p.num_qblocks - 1 - k : k) : k;
+    const int qb = mask_is_causal(MASK) ? (i == 0 ? p.num_qblocks - 1 - k : k) : k;
     w.q0 = qb * BM;
     w.kv_len = p.m;
-    if (MASK == MASK_KEY_PADDING) {
+    if (mask_has_lengths(MASK)) {
         const int len = __ldg(p.key_lengths + w.bh / p.H);
         w.kv_len = len < 0 ? 0 : (len > p.m ? p.m : len);
     }
-    if (MASK == MASK_CAUSAL) {
-        const int last = min(w.q0 + BM - 1, p.n - 1);
-        w.nkv = min(last / BN + 1, (w.kv_len + BN - 1) / BN);
-    } else {
-        w.nkv = (w.kv_len + BN - 1) / BN;
+    w.nkv = (w.kv_len + BN - 1) / BN;
+    if (mask_is_causal(MASK)) {
+        // the last key visible to the tile's last row; none if it is negative
+        const int last = min(w.q0 + BM - 1, p.n - 1) + p.causal_off;
+        w.nkv = last < 0 ? 0 : min(last / BN + 1, w.nkv);
     }
     return w;
 }
@@ -164,13 +170,13 @@ __device__ __forceinline__ void advance(TilePos& t, int u_step, const FwdParams&
     }
 }
 
-template <int D, int MASK>
-__global__ void __launch_bounds__(Layout<D>::NUM_THREADS, Layout<D>::CTAS_PER_SM)
+template <int DK, int DV, int MASK>
+__global__ void __launch_bounds__(Layout<DK, DV>::NUM_THREADS, Layout<DK, DV>::CTAS_PER_SM)
 attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                    const FwdParams p)
 {
-    using L = Layout<D>;
+    using L = Layout<DK, DV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -240,9 +246,9 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     !mbar_wait(bar(L::B_KEMPTY + s), static_cast<uint32_t>(kc / L::KS - 1) & 1u,
                                abort_word, p.status, STATUS_TMA_WAIT, limit))
                     return false;
-                mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::TILE);
-                for (int c = 0; c < L::CH; ++c)
-                    tma_load_3d(sK + s * L::TILE + c * CHUNK_BYTES, &tmK, bar(L::B_KFULL + s), c * 64,
+                mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::TILE_K);
+                for (int c = 0; c < L::CHK; ++c)
+                    tma_load_3d(sK + s * L::TILE_K + c * CHUNK_BYTES, &tmK, bar(L::B_KFULL + s), c * 64,
                                 j * BN, bh);
                 ++kc;
                 return true;
@@ -253,9 +259,9 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     !mbar_wait(bar(L::B_VEMPTY + s), static_cast<uint32_t>(vc / L::VS - 1) & 1u,
                                abort_word, p.status, STATUS_TMA_WAIT, limit))
                     return false;
-                mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::TILE);
-                for (int c = 0; c < L::CH; ++c)
-                    tma_load_3d(sV + s * L::TILE + c * CHUNK_BYTES, &tmV, bar(L::B_VFULL + s), c * 64,
+                mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::TILE_V);
+                for (int c = 0; c < L::CHV; ++c)
+                    tma_load_3d(sV + s * L::TILE_V + c * CHUNK_BYTES, &tmV, bar(L::B_VFULL + s), c * 64,
                                 j * BN, bh);
                 ++vc;
                 return true;
@@ -269,8 +275,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(L::B_QFULL), L::TILE);
-                for (int c = 0; c < L::CH; ++c)
+                mbar_arrive_expect_tx(bar(L::B_QFULL), L::TILE_K);
+                for (int c = 0; c < L::CHK; ++c)
                     tma_load_3d(sQ + c * CHUNK_BYTES, &tmQ, bar(L::B_QFULL), c * 64, w.q0, w.bh);
                 ++qc;
                 // K(j+1) is issued before V(j): S(j+1) needs it while P(j) is computed
@@ -292,7 +298,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             // lane issues each tcgen05 instruction. Descriptors are formed once per
             // buffer and advanced by adding the encoded byte offset (address >> 4).
             constexpr uint32_t ID_S = idesc_bf16_f32(BM, BN, false, false);
-            constexpr uint32_t ID_PV = idesc_bf16_f32(BM, D, false, true);
+            constexpr uint32_t ID_PV = idesc_bf16_f32(BM, DV, false, true);
             const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
             const uint64_t dK0 = sdesc_sw128(sK, 16, 1024);
             const uint64_t dV0 = sdesc_sw128(sV, CHUNK_BYTES, 1024);
@@ -302,10 +308,10 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 return __all_sync(0xffffffffu, r);
             };
             auto issue_S = [&](int s) {
-                const uint64_t dK = dK0 + static_cast<uint64_t>((s * L::TILE) >> 4);
-                const uint32_t qt = tmem + L::QT_COL + static_cast<uint32_t>((qc - 1) & 1) * (D / 2);
+                const uint64_t dK = dK0 + static_cast<uint64_t>((s * L::TILE_K) >> 4);
+                const uint32_t qt = tmem + L::QT_COL + static_cast<uint32_t>((qc - 1) & 1) * (DK / 2);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>(((kk / 4) * CHUNK_BYTES + (kk % 4) * 32) >> 4);
                     if (L::Q_IN_TMEM)
                         mma_ts_warp(tmem + L::S_COL, qt + kk * 8, dK + off, ID_S, kk > 0 ? 1u : 0u);
@@ -314,7 +320,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
             };
             auto issue_PV = [&](int s, bool acc) {
-                const uint64_t dV = dV0 + static_cast<uint64_t>((s * L::TILE) >> 4);
+                const uint64_t dV = dV0 + static_cast<uint64_t>((s * L::TILE_V) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk)
                     mma_ts_warp(tmem + L::O_COL, tmem + L::P_COL + kk * 8, dV + static_cast<uint64_t>((kk * 2048) >> 4),
@@ -390,9 +396,9 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                   STATUS_SOFTMAX_WAIT, limit);
             w_ok = __all_sync(0xffffffffu, w_ok);
             if (!w_ok) return false;
-            const uint32_t qt = tmem + lane_base + L::QT_COL + static_cast<uint32_t>(qc & 1) * (D / 2);
+            const uint32_t qt = tmem + lane_base + L::QT_COL + static_cast<uint32_t>(qc & 1) * (DK / 2);
 #pragma unroll
-            for (int c = 0; c < L::CH; ++c) {
+            for (int c = 0; c < L::CHK; ++c) {
                 uint32_t q[32];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
@@ -416,6 +422,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (TilePos t = first_tile; ok && t.u < p.num_units; advance<MASK>(t, u_step, p)) {
             const Unit w = tile_of<MASK>(t.u, t.ti, p);
             const int qrow = w.q0 + r;
+            const int qlim = qrow + p.causal_off;   // last key this row sees under the causal mask
             float m_ref = -INFINITY;
             float l_run = 0.f;
             if (L::Q_IN_TMEM && w.nkv > 0 && !(q_done.u == t.u && q_done.ti == t.ti)) {
@@ -445,12 +452,12 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(sr[c]);
                 const int key0 = j * BN;
                 const bool need_mask = __any_sync(
-                    0xffffffffu, (key0 + BN > w.kv_len) || (MASK == MASK_CAUSAL && key0 + BN - 1 > qrow));
+                    0xffffffffu, (key0 + BN > w.kv_len) || (mask_is_causal(MASK) && key0 + BN - 1 > qlim));
                 if (need_mask) {
 #pragma unroll
                     for (int c = 0; c < BN; ++c) {
                         const int key = key0 + c;
-                        if (key >= w.kv_len || (MASK == MASK_CAUSAL && key > qrow)) s[c] = -INFINITY;
+                        if (key >= w.kv_len || (mask_is_causal(MASK) && key > qlim)) s[c] = -INFINITY;
                     }
                 }
                 // row maximum: eight independent chains of three-input max
@@ -499,7 +506,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                    for (int cc = 0; cc < DV / 32; ++cc) {
                         uint32_t o[32];
                         tmem_ld32(tO + 32 * cc, o);
                         tmem_wait_ld();
@@ -546,7 +553,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             if (store_pending && lane == 0) bulk_wait_group_read0();
             __syncwarp();
 #pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
+            for (int cc = 0; cc < DV / 32; ++cc) {
                 uint32_t o[32];
                 if (w.nkv > 0) {
                     tmem_ld32(tO + 32 * cc, o);
@@ -575,7 +582,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && w.q0 + 32 * warp < p.n) {
-                for (int c = 0; c < L::CH; ++c)
+                for (int c = 0; c < L::CHV; ++c)
                     tma_store_3d(&tmO, sO + c * CHUNK_BYTES + warp * 32 * 128, c * 64, w.q0 + 32 * warp, w.bh);
                 bulk_commit_group();
                 store_pending = true;
@@ -594,11 +601,11 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
 }
 
-template <int D, int MASK>
+template <int DK, int DV, int MASK>
 cudaError_t launch(const TensorMaps& maps, const FwdParams& p, int num_sms, cudaStream_t stream)
 {
-    using L = Layout<D>;
-    auto kern = attn_fwd_dp_kernel<D, MASK>;
+    using L = Layout<DK, DV>;
+    auto kern = attn_fwd_dp_kernel<DK, DV, MASK>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -31,6 +31,18 @@ MASK_KINDS = (MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING)
 LENGTH_MASKS = (MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING)
 
 
+def nominal_pairs(n: int, m: int, mask: str) -> float:
+    """(query, key) pairs a FLOP count charges: n*m, or under a causal mask the
+    visible part with the masked triangle counted as half its square (n*m - n*n/2
+    for n <= m, m*m/2 for n > m), the usual convention that charges a square
+    causal mask n*m/2."""
+    if mask not in (MASK_CAUSAL, MASK_CAUSAL_KEY_PADDING):
+        return float(n) * m
+    if n <= m:
+        return float(n) * m - float(n) * n / 2
+    return float(m) * m / 2
+
+
 @dataclasses.dataclass(frozen=True)
 class Workload:
     """One seeded attention workload: shapes, mask, value recipe and seed."""
@@ -51,9 +63,9 @@ class Workload:
     d_model: int = 0                # projection recipe only
 
     def flops(self) -> float:
-        """Nominal forward FLOPs: two GEMMs of 2*n*m*d each, halved for causal."""
-        f = 4.0 * self.B * self.H * self.n * self.m * self.d_k
-        return f / 2 if self.mask in (MASK_CAUSAL, MASK_CAUSAL_KEY_PADDING) else f
+        """Nominal forward FLOPs: 2*d_k (scores) + 2*d_v (weighted sum) per visible
+        (query, key) pair (``nominal_pairs``; half of n*m for a square causal mask)."""
+        return 2.0 * self.B * self.H * (self.d_k + self.d_v) * nominal_pairs(self.n, self.m, self.mask)
 
     def io_bytes(self) -> int:
         """Algorithmic HBM bytes: Q, K, V read once (bf16); O (bf16) and LSE (fp32) written once."""
@@ -80,6 +92,19 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = ["tiny_encoder", "base_encoder_keypad", "big_decoder_causal",
                   "cross_keypad", "long_causal"]
+
+# Mask and shape variants at the sizes of the workloads above: the decoder target
+# mask (causal and key padding, "Transformer 详解" §5.3) at big-decoder sizes with
+# key lengths in [512, 1024]; 1024 new query rows against 8192 keys under the
+# causal mask (bottom-right) at d 128; value heads twice as wide as the key heads.
+WORKLOADS.update({
+    "decoder_target_mask": Workload("decoder_target_mask", 16, 16, 1024, 1024, 64, 64,
+                                    MASK_CAUSAL_KEY_PADDING, seed=5, len_lo=512, len_hi=1024),
+    "prefill_continuation": Workload("prefill_continuation", 4, 16, 1024, 8192, 128, 128,
+                                     MASK_CAUSAL, seed=6, value_scale=0.5),
+    "wide_values": Workload("wide_values", 16, 16, 1024, 1024, 64, 128, MASK_NONE, seed=7),
+})
+VARIANT_ORDER = ["decoder_target_mask", "prefill_continuation", "wide_values"]
 
 
 @dataclasses.dataclass
@@ -154,8 +179,8 @@ def workload_inputs(w: Workload | str) -> Inputs:
         return make_projection_inputs(w.B, w.H, w.n, w.d_model, w.mask, w.seed, w.len_lo, w.len_hi)
     return make_inputs(w.B, w.H, w.n, w.m, w.d_k, w.d_v, w.mask, w.seed,
                        value_scale=w.value_scale,
-                       len_lo=w.len_lo if w.mask == MASK_KEY_PADDING else None,
-                       len_hi=w.len_hi if w.mask == MASK_KEY_PADDING else None)
+                       len_lo=w.len_lo if w.mask in LENGTH_MASKS else None,
+                       len_hi=w.len_hi if w.mask in LENGTH_MASKS else None)
 
 
 def sample_rows(B, H, n, count, seed):
