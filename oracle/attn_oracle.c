@@ -48,7 +48,20 @@
  * Layouts: Q [B,H,n,dk], K [B,H,m,dk], V [B,H,m,dv], O [B,H,n,dv], LSE
  * [B,H,n], all contiguous row-major fp64; key_lengths int32 [B].
  *
- * ORACLE_PLANT (compile-time, default 0, 1..8) plants one known mistake so that the
+ * Backward (oracle_attn_bwd). For a loss whose gradient with respect to O is
+ * dO, the chain rule through the definition above gives, per head and row i
+ * with at least one visible key (w_j the weights of row i, 0 when masked):
+ *
+ *   dV_j  += w_j dO_i                                  (o_i = sum_j w_j v_j)
+ *   dP_j   = dO_i . v_j
+ *   dS_j   = w_j (dP_j - D_i),  D_i = sum_j w_j dP_j   (softmax Jacobian:
+ *            dw_j/ds_k = w_j (delta_jk - w_k); D_i also equals dO_i . o_i)
+ *   dQ_i   = scale sum_j dS_j k_j,  dK_j += scale dS_j q_i   (s_j = scale q_i.k_j)
+ *
+ * Rows with no visible key contribute nothing (their o_i = 0 is constant).
+ * Masked keys get dK_j = dV_j = 0.
+ *
+ * ORACLE_PLANT (compile-time, default 0, 1..11) plants one known mistake so that the
  * test suite can show that its pins catch it; the shipped build never sets it.
  */
 #include <math.h>
@@ -258,6 +271,95 @@ static int run(job_t base)
     return rc;
 }
 
+/*
+ * Backward of one head. Qh [n,dk], Kh [m,dk], Vh [m,dv], dOh [n,dv]; writes
+ * dQh [n,dk], dKh [m,dk], dVh [m,dv]. w, dp are scratch of m doubles, o of dv.
+ */
+static void head_bwd(const double* Qh, const double* Kh, const double* Vh, const double* dOh,
+                     int64_t n, int64_t m, int dk, int dv, int mask_kind, int64_t len, double scale,
+                     double* dQh, double* dKh, double* dVh, double* w, double* dp, double* o)
+{
+    for (int64_t t = 0; t < m * dk; ++t) dKh[t] = 0.0;
+    for (int64_t t = 0; t < m * dv; ++t) dVh[t] = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double* q = Qh + i * dk;
+        const double* g = dOh + i * dv;
+        double* dq = dQh + i * dk;
+        double lse;
+        for (int c = 0; c < dk; ++c) dq[c] = 0.0;
+        /* forward of row i: on return w holds its weights (0 where masked) */
+        attn_row(q, Kh, Vh, m, dk, dv, mask_kind, i, len, m - n, scale, w, o, &lse, NULL);
+        if (isinf(lse)) continue;          /* no visible key: o_i = 0 is constant */
+        double D = 0.0;
+        for (int64_t j = 0; j < m; ++j) {
+            double acc = 0.0;
+            const double* v = Vh + j * dv;
+            for (int c = 0; c < dv; ++c) acc += g[c] * v[c];
+            dp[j] = acc;
+            D += w[j] * acc;
+        }
+        for (int64_t j = 0; j < m; ++j) {
+            if (w[j] == 0.0) continue;
+#if ORACLE_PLANT == 9
+            double ds = w[j] * dp[j];                      /* planted: D_i dropped */
+#else
+            double ds = w[j] * (dp[j] - D);
+#endif
+            const double* k = Kh + j * dk;
+            double* dk_j = dKh + j * dk;
+            double* dv_j = dVh + j * dv;
+            for (int c = 0; c < dk; ++c) {
+                dq[c] += scale * ds * k[c];
+#if ORACLE_PLANT == 10
+                dk_j[c] += ds * q[c];                      /* planted: scale dropped in dK */
+#else
+                dk_j[c] += scale * ds * q[c];
+#endif
+            }
+#if ORACLE_PLANT == 11
+            for (int c = 0; c < dv; ++c) dv_j[c] += w[j] * o[c];  /* planted: O in place of dO */
+#else
+            for (int c = 0; c < dv; ++c) dv_j[c] += w[j] * g[c];
+#endif
+        }
+    }
+}
+
+typedef struct {
+    const double *Q, *K, *V, *dO;
+    const int32_t* key_lengths;
+    int64_t B, H, n, m;
+    int dk, dv, mask_kind;
+    double scale;
+    double *dQ, *dK, *dV;
+    int nthreads, tid;
+} bwd_job_t;
+
+static void* bwd_worker(void* arg)
+{
+    bwd_job_t* jb = (bwd_job_t*)arg;
+    size_t mm = (size_t)(jb->m > 0 ? jb->m : 1);
+    double* w = (double*)malloc(sizeof(double) * mm);
+    double* dp = (double*)malloc(sizeof(double) * mm);
+    double* o = (double*)malloc(sizeof(double) * (size_t)jb->dv);
+    void* ret = NULL;
+    if (!w || !dp || !o) {
+        ret = (void*)1;
+    } else {
+        for (int64_t bh = jb->tid; bh < jb->B * jb->H; bh += jb->nthreads) {
+            int64_t len = clamp_len(jb->key_lengths, jb->mask_kind, bh / jb->H, jb->m);
+            head_bwd(jb->Q + bh * jb->n * jb->dk, jb->K + bh * jb->m * jb->dk,
+                     jb->V + bh * jb->m * jb->dv, jb->dO + bh * jb->n * jb->dv, jb->n, jb->m,
+                     jb->dk, jb->dv, jb->mask_kind, len, jb->scale, jb->dQ + bh * jb->n * jb->dk,
+                     jb->dK + bh * jb->m * jb->dk, jb->dV + bh * jb->m * jb->dv, w, dp, o);
+        }
+    }
+    free(w);
+    free(dp);
+    free(o);
+    return ret;
+}
+
 static int bad_args(int64_t B, int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind)
 {
     return B < 0 || H < 0 || n < 0 || m < 0 || dk < 1 || dv < 1 || mask_kind < 0 ||
@@ -292,4 +394,35 @@ int oracle_attn_rows(const double* Q, const double* K, const double* V, int64_t 
     job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, O, LSE, NULL,
                 rows, nrows, nthreads, 0};
     return run(jb);
+}
+
+/* Backward: dQ [B,H,n,dk], dK [B,H,m,dk], dV [B,H,m,dv] for the upstream
+ * gradient dO [B,H,n,dv]. Returns 0 on success. */
+int oracle_attn_bwd(const double* Q, const double* K, const double* V, const double* dO,
+                    int64_t B, int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind,
+                    const int32_t* key_lengths, double scale, double* dQ, double* dK, double* dV,
+                    int nthreads)
+{
+    if (bad_args(B, H, n, m, dk, dv, mask_kind)) return -1;
+    if (uses_lengths(mask_kind) && key_lengths == NULL) return -1;
+    int nt = nthreads < 1 ? 1 : (nthreads > 1024 ? 1024 : nthreads);
+    pthread_t th[1024];
+    bwd_job_t jobs[1024];
+    int rc = 0, started = 0;
+    for (int t = 0; t < nt; ++t) {
+        bwd_job_t jb = {Q, K, V, dO, key_lengths, B, H, n, m, dk, dv, mask_kind, scale,
+                        dQ, dK, dV, nt, t};
+        jobs[t] = jb;
+    }
+    if (nt == 1) return bwd_worker(&jobs[0]) == NULL ? 0 : -1;
+    for (int t = 0; t < nt; ++t) {
+        if (pthread_create(&th[t], NULL, bwd_worker, &jobs[t]) != 0) { rc = -1; break; }
+        ++started;
+    }
+    for (int t = 0; t < started; ++t) {
+        void* ret = NULL;
+        pthread_join(th[t], &ret);
+        if (ret != NULL) rc = -1;
+    }
+    return rc;
 }

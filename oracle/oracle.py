@@ -66,6 +66,9 @@ def _load(plant: int = 0) -> ctypes.CDLL:
     lib.oracle_attn_rows.argtypes = [dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p,
                                      ctypes.c_double, i64p, i64, dp, dp, ci]
     lib.oracle_attn_rows.restype = ci
+    lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p,
+                                    ctypes.c_double, dp, dp, dp, ci]
+    lib.oracle_attn_bwd.restype = ci
     _libs[plant] = lib
     return lib
 
@@ -151,3 +154,25 @@ def attn_rows(Q, K, V, rows, mask="none", key_lengths=None, scale=None, *, threa
     if rc != 0:
         raise RuntimeError(f"oracle_attn_rows failed ({rc})")
     return O, L
+
+
+def attn_bwd(Q, K, V, dO, mask="none", key_lengths=None, scale=None, *, threads=None, plant=0):
+    """Oracle backward for the upstream gradient dO [B,H,n,dv]: returns (dQ [B,H,n,dk],
+    dK [B,H,m,dk], dV [B,H,m,dv]) in fp64. ``scale`` defaults to 1/sqrt(d_k)."""
+    Qd, Kd, Vd, dOd = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    B, H, n, m, dk, dv = _shapes(Qd, Kd, Vd)
+    if dOd.shape != (B, H, n, dv):
+        raise ValueError("dO must be [B, H, n, d_v]")
+    sc = 1.0 / np.sqrt(dk) if scale is None else float(scale)
+    lens = _lens(key_lengths, B)
+    dQ = np.zeros((B, H, n, dk))
+    dK = np.zeros((B, H, m, dk))
+    dV = np.zeros((B, H, m, dv))
+    rc = _load(plant).oracle_attn_bwd(
+        _ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
+        _ptr(dOd, ctypes.c_double), B, H, n, m, dk, dv, MASK_CODES[mask],
+        _ptr(lens, ctypes.c_int32), sc, _ptr(dQ, ctypes.c_double), _ptr(dK, ctypes.c_double),
+        _ptr(dV, ctypes.c_double), threads or min(default_threads(), 16))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd failed ({rc})")
+    return dQ, dK, dV
