@@ -48,6 +48,7 @@
 #ifndef ATTN_SM103A_H
 #define ATTN_SM103A_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -141,6 +142,42 @@ void attn_set_watchdog(uint64_t limit_ns, uint32_t debug_flags);
 int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
                      int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O,
                      float* LSE, void* stream);
+
+/*
+ * Attention backward: the gradients of the forward above for an upstream
+ * gradient dO. The pages print the forward only; the backward is the chain
+ * rule through it (training is the pages' motivation): with P the attention
+ * weights (0 where masked),
+ *
+ *     dV = Pᵀ dO,   dS = P ∘ (dO Vᵀ - D),  D_i = dO_i · O_i,
+ *     dQ = scale * dS K,   dK = scale * dSᵀ Q.
+ *
+ * P is recomputed from Q, K and the forward's LSE; D from the forward's O.
+ *   Q, K, V      the forward's inputs (bf16, layouts as in attn_fwd).
+ *   O, LSE       the forward's outputs for these inputs (bf16 [B,H,n,d_v],
+ *                fp32 [B,H,n]); LSE may not be NULL.
+ *   dO           bf16 [B,H,n,d_v], the gradient of the loss with respect to O.
+ *   B..scale     as in attn_fwd; supported: d_k == d_v in {64, 128}.
+ *   dQ, dK, dV   bf16 outputs [B,H,n,d_k], [B,H,m,d_k], [B,H,m,d_v]. Keys that
+ *                no query sees (masked for every row) get exactly 0. n = 0
+ *                writes dK = dV = 0; m = 0 writes dQ = 0.
+ *   workspace    device scratch owned by the caller, 256-byte aligned, at least
+ *                attn_bwd_workspace_size(...) bytes (an fp32 dQ accumulator and
+ *                two fp32 per-row vectors); its contents on entry do not
+ *                matter. Not needed (may be NULL) when n = 0 or m = 0.
+ * Three kernels run on `stream`: a preparation kernel (D, LSE·log2 e, zeroing the
+ * accumulator), the main kernel (one CTA per (b, h, 128-key tile)), and the
+ * conversion of dQ to bf16. The dQ accumulation order across key tiles is not
+ * fixed, so dQ may differ in its last bits between runs; dK and dV do not.
+ * Returns ATTN_OK or a negative attn_status_t (ATTN_ERR_INVALID_ARG also for a
+ * workspace that is too small); on error nothing is enqueued.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int n, int m, int d_k, int d_v);
+
+int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+             const float* LSE, int B, int H, int n, int m, int d_k, int d_v, int mask_kind,
+             const int32_t* key_lengths, float scale, void* dQ, void* dK, void* dV,
+             void* workspace, size_t workspace_bytes, void* stream);
 
 /* Human-readable name of a status code. */
 const char* attn_status_string(int status);

@@ -103,3 +103,41 @@ def test_flop_model():
     assert attn.flops(1, 1, 256, 1024, 64, "causal") == 4.0 * 64 * (256 * 1024 - 256 * 256 / 2)
     assert attn.flops(1, 1, 1024, 256, 64, "causal") == 4.0 * 64 * 256 * 256 / 2
     assert attn.flops(2, 3, 128, 96, 64, "none", d_v=128) == 2.0 * 2 * 3 * (64 + 128) * 128 * 96
+
+
+def call_bwd(B=1, H=1, n=4, m=4, dk=64, dv=64, mask=0, lens=None, dQ=P2, dK=P2, dV=P2, ws=P,
+             ws_bytes=1 << 20, Q=P, O=P, LSE=P):
+    return attn.attn_bwd_raw(Q, P, P, O, P, LSE, B, H, n, m, dk, dv, mask, lens, -1.0, dQ, dK, dV, ws,
+                             ws_bytes, 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=2, lens=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=3, lens=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dk=64, dv=128), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dk=96, dv=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dQ=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dK=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ws=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(LSE=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ws_bytes=16), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ws=ctypes.c_void_p(0x10080)), attn.ATTN_ERR_MISALIGNED),
+    (dict(dQ=ctypes.c_void_p(0x20008)), attn.ATTN_ERR_MISALIGNED),
+    (dict(O=ctypes.c_void_p(0x20002)), attn.ATTN_ERR_MISALIGNED),
+])
+def test_bwd_rejects_bad_arguments(lib, kw, code):
+    assert call_bwd(**kw) == code
+
+
+def test_bwd_workspace_size():
+    # dQ accumulator (fp32) + two fp32 vectors over 128-padded rows, each 256-byte aligned
+    assert attn.bwd_workspace_size(2, 3, 100, 50, 64, 64) == 2 * 3 * 100 * 64 * 4 + 2 * 3072
+    assert attn.bwd_workspace_size(0, 3, 100, 50, 64, 64) == 0
+    assert attn.bwd_workspace_size(1, 1, 129, 7, 128, 128) == 129 * 128 * 4 + 2 * 1024
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0)])
+def test_bwd_empty_problem_is_a_noop(lib, kw):
+    assert call_bwd(**kw) == attn.ATTN_OK

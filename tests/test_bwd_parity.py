@@ -1,0 +1,154 @@
+"""GPU parity of the attention backward (dQ, dK, dV) against the fp64 CPU oracle.
+
+The GPU runs its own forward first (O in bf16, LSE in fp32) and differentiates
+from those, as a training step would; the oracle differentiates the exact
+function of the same bf16 inputs. Tolerance, derived from the path's roundings
+(every other error source is below 2^-18 relative): for each gradient G,
+elementwise |G - G_ref| <= 2 * bound + 1e-6 with
+
+  dV: bound = 2^-9 |dV_ref| + 2^-9 (Wᵀ |dO|)        (bf16 output; bf16 P)
+  dK: bound = 2^-9 |dK_ref| + scale * Tᵀ |Q|
+  dQ: bound = 2^-9 |dQ_ref| + scale * T |K|
+      T_ij  = W_ij (2^-9 |dP_ij - D_i| + E_i)        (bf16 dS; D from the bf16 O)
+      E_i   = 2^-8 sum_c |dO_ic| (|O_ic| + A_ic)     (the forward's O error)
+
+where W are the oracle's weights, dP = dO Vᵀ, D_i = dO_i . O_i, and A = the
+oracle's output on |V| (the sum of w_j |v_j| that bounds the forward's P
+rounding). The factor 2 covers the first-order derivation.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from transformer_scaled_dot_03_gb300 import attn, build, inputs
+
+pytestmark = pytest.mark.gpu
+
+HALF_ULP = 2.0 ** -9
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return attn.load()
+
+
+def run_gpu_bwd(x: inputs.Inputs, dO: torch.Tensor):
+    Q, K, V, g = x.Q.cuda(), x.K.cuda(), x.V.cuda(), dO.cuda()
+    lens = x.key_lengths.cuda() if x.key_lengths is not None else None
+    O, LSE = attn.attn_fwd(Q, K, V, x.mask, lens, x.scale)
+    dQ, dK, dV = attn.attn_bwd(Q, K, V, O, LSE, g, x.mask, lens, x.scale)
+    rc, detail = attn.device_status()
+    assert rc == attn.ATTN_OK, (rc, detail)
+    torch.cuda.synchronize()
+    return tuple(t.float().cpu().numpy() for t in (dQ, dK, dV))
+
+
+def bounds(x: inputs.Inputs, dO: torch.Tensor, refs):
+    Qd, Kd, Vd, g = (t.double().numpy() for t in (x.Q, x.K, x.V, dO))
+    Or, _, W = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale, weights=True)
+    A, _ = oracle.attn_fwd(x.Q, x.K, x.V.abs(), x.mask, x.key_lengths, x.scale)
+    dP = np.einsum("bhic,bhjc->bhij", g, Vd)
+    D = np.sum(g * Or, axis=-1)
+    E = 2.0 ** -8 * np.sum(np.abs(g) * (np.abs(Or) + A), axis=-1)
+    T = W * (HALF_ULP * np.abs(dP - D[..., None]) + E[..., None])
+    dQr, dKr, dVr = refs
+    bq = HALF_ULP * np.abs(dQr) + x.scale * np.einsum("bhij,bhjc->bhic", T, np.abs(Kd))
+    bk = HALF_ULP * np.abs(dKr) + x.scale * np.einsum("bhij,bhic->bhjc", T, np.abs(Qd))
+    bv = HALF_ULP * np.abs(dVr) + HALF_ULP * np.einsum("bhij,bhic->bhjc", W, np.abs(g))
+    return bq, bk, bv
+
+
+def check_bwd(x: inputs.Inputs, dO: torch.Tensor, label=""):
+    got = run_gpu_bwd(x, dO)
+    refs = oracle.attn_bwd(x.Q, x.K, x.V, dO, x.mask, x.key_lengths, x.scale)
+    for name, G, R, bd in zip(("dQ", "dK", "dV"), got, refs, bounds(x, dO, refs)):
+        assert np.all(np.isfinite(G)), f"{label}: non-finite {name}"
+        excess = np.abs(G - R) - (2 * bd + 1e-6)
+        worst = np.unravel_index(np.argmax(excess), excess.shape)
+        assert excess.max() <= 0, (f"{label}: {name} exceeds its bound by {excess.max():.3e} at {worst} "
+                                   f"(got {G[worst]:.5f}, ref {R[worst]:.5f}, bound {2 * bd[worst]:.2e})")
+    return got, refs
+
+
+def case(B, H, n, m, d, mask, seed, lens=None, value_scale=1.0):
+    x = inputs.make_inputs(B, H, n, m, d, d, mask, seed=seed, key_lengths=lens, value_scale=value_scale)
+    dO = inputs.make_grad_output(B, H, n, d, seed=seed + 1)
+    return x, dO
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask,n,m,lens", [
+    ("none", 200, 200, None),
+    ("none", 1, 300, None),
+    ("none", 300, 77, None),
+    ("causal", 256, 256, None),
+    ("causal", 130, 300, None),
+    ("causal", 300, 130, None),
+    ("key_padding", 150, 260, [260, 1, 0, 129]),
+    ("causal_key_padding", 200, 200, [200, 128, 5, 0]),
+    ("causal_key_padding", 100, 333, [333, 250, 234, 1]),
+])
+def test_bwd_matches_oracle(d, mask, n, m, lens):
+    B = len(lens) if lens else 2
+    x, dO = case(B, 2, n, m, d, mask, seed=8000 + n + m + d, lens=lens)
+    check_bwd(x, dO, f"{mask} n={n} m={m} d={d}")
+
+
+def test_bwd_big_decoder_small_batch():
+    """Big-decoder sizes (n = m = 1024, d 64, causal) on 2 x 4 heads, every element."""
+    x, dO = case(2, 4, 1024, 1024, 64, "causal", seed=8100)
+    check_bwd(x, dO, "big decoder")
+
+
+def test_bwd_long_d128_small_batch():
+    """d 128, n = m = 2048, causal, x0.5 inputs (the long-context recipe), 1 x 2 heads."""
+    x, dO = case(1, 2, 2048, 2048, 128, "causal", seed=8200, value_scale=0.5)
+    check_bwd(x, dO, "long d128")
+
+
+def test_bwd_sharp_rows():
+    """Q and K scaled by 8: nearly one-hot rows, large dS spread."""
+    x, dO = case(2, 2, 256, 384, 64, "key_padding", seed=8300, lens=[384, 200])
+    x.Q = (x.Q.float() * 8).to(torch.bfloat16)
+    x.K = (x.K.float() * 8).to(torch.bfloat16)
+    check_bwd(x, dO, "sharp")
+
+
+def test_bwd_full_size_identities():
+    """Big-decoder workload at full size (16 x 16 heads) under the decoder target mask:
+    the softmax identities hold on the GPU's gradients (dK sums to zero over the keys
+    of a head; dV sums to the dO of the rows that see a key), and one head matches
+    the oracle element by element."""
+    B, H, n, d = 16, 16, 1024, 64
+    x = inputs.make_inputs(B, H, n, n, d, d, "causal_key_padding", seed=8400, len_lo=512, len_hi=n)
+    dO = inputs.make_grad_output(B, H, n, d, seed=8401)
+    dQ, dK, dV = run_gpu_bwd(x, dO)
+    for G in (dQ, dK, dV):
+        assert np.all(np.isfinite(G))
+    g = dO.double().numpy()
+    # dK: the column sums cancel; compare against the sum of magnitudes it cancels from
+    scale_k = np.abs(dK).sum(axis=2)
+    assert np.all(np.abs(dK.sum(axis=2)) <= 2.0 ** -6 * scale_k + 1e-3)
+    dv_sum = dV.sum(axis=2)
+    np.testing.assert_allclose(dv_sum, g.sum(axis=2), atol=2.0 ** -6 * np.abs(g).sum(axis=2).max())
+    b, h = 5, 11
+    xs = inputs.Inputs(x.Q[b:b + 1, h:h + 1].contiguous(), x.K[b:b + 1, h:h + 1].contiguous(),
+                       x.V[b:b + 1, h:h + 1].contiguous(), x.key_lengths[b:b + 1].clone(), x.mask, x.scale)
+    gs = dO[b:b + 1, h:h + 1].contiguous()
+    refs = oracle.attn_bwd(xs.Q, xs.K, xs.V, gs, xs.mask, xs.key_lengths, xs.scale)
+    for name, G, R, bd in zip(("dQ", "dK", "dV"), (dQ[b:b + 1, h:h + 1], dK[b:b + 1, h:h + 1],
+                                                   dV[b:b + 1, h:h + 1]), refs, bounds(xs, gs, refs)):
+        assert np.all(np.abs(G - R) <= 2 * bd + 1e-6), name
+
+
+def test_bwd_dk_dv_deterministic():
+    x, dO = case(2, 3, 300, 300, 64, "causal", seed=8500)
+    a = run_gpu_bwd(x, dO)
+    b = run_gpu_bwd(x, dO)
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    assert np.max(np.abs(a[0] - b[0])) <= 2.0 ** -7 * max(1.0, float(np.abs(a[0]).max()))

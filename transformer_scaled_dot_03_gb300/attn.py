@@ -33,7 +33,7 @@ MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PAD
 
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
-           "attn_last_error", "attn_fwd_noalloc")
+           "attn_last_error", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +64,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_set_watchdog.restype = None
         lib.attn_status_string.argtypes = [i32]
         lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32,
+                                 vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.attn_bwd.restype = i32
+        lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         _lib = lib
@@ -130,6 +135,65 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "non
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd", last_error() if rc == ATTN_ERR_CUDA else "")
     return O, LSE
+
+
+def attn_bwd_raw(Q_ptr, K_ptr, V_ptr, O_ptr, dO_ptr, LSE_ptr, B, H, n, m, d_k, d_v, mask_kind,
+                 key_lengths_ptr, scale, dQ_ptr, dK_ptr, dV_ptr, ws_ptr, ws_bytes, stream_handle) -> int:
+    """The C backward entry point with plain integers/pointers; returns the status code."""
+    return load().attn_bwd(Q_ptr, K_ptr, V_ptr, O_ptr, dO_ptr, LSE_ptr, int(B), int(H), int(n), int(m),
+                           int(d_k), int(d_v), int(mask_kind), key_lengths_ptr, ctypes.c_float(scale),
+                           dQ_ptr, dK_ptr, dV_ptr, ws_ptr, ctypes.c_size_t(ws_bytes),
+                           ctypes.c_void_p(stream_handle))
+
+
+def bwd_workspace_size(B, H, n, m, d_k, d_v) -> int:
+    return int(load().attn_bwd_workspace_size(int(B), int(H), int(n), int(m), int(d_k), int(d_v)))
+
+
+def attn_bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE: torch.Tensor,
+             dO: torch.Tensor, mask: str = "none", key_lengths: torch.Tensor | None = None,
+             scale: float | None = None, dQ: torch.Tensor | None = None, dK: torch.Tensor | None = None,
+             dV: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Attention backward on the GPU: (dQ, dK, dV) bf16 for the upstream gradient dO, given
+    the forward's inputs Q, K, V and outputs O (bf16) and LSE (fp32). ``workspace`` (uint8
+    CUDA tensor of at least ``bwd_workspace_size`` bytes) is allocated here when omitted.
+    Asynchronous on ``stream`` (default: PyTorch's current stream)."""
+    if mask not in MASK_CODES:
+        raise ValueError(f"unknown mask {mask!r}")
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    B, H, n, d_k = Q.shape
+    m = K.shape[2]
+    d_v = V.shape[3]
+    if tuple(K.shape) != (B, H, m, d_k) or tuple(V.shape[:3]) != (B, H, m) \
+            or tuple(O.shape) != (B, H, n, d_v) or tuple(dO.shape) != (B, H, n, d_v):
+        raise ValueError("inconsistent Q/K/V/O/dO shapes")
+    if LSE.dtype != torch.float32 or not LSE.is_cuda or tuple(LSE.shape) != (B, H, n) \
+            or not LSE.is_contiguous():
+        raise ValueError("LSE must be a contiguous fp32 CUDA tensor [B, H, n]")
+    uses_lengths = mask in _inputs.LENGTH_MASKS
+    if uses_lengths and (key_lengths is None or key_lengths.dtype != torch.int32
+                         or not key_lengths.is_cuda or key_lengths.numel() != B
+                         or not key_lengths.is_contiguous()):
+        raise ValueError(f"{mask} needs key_lengths: contiguous int32 CUDA [B]")
+    dev = Q.device
+    dQ = torch.empty((B, H, n, d_k), dtype=torch.bfloat16, device=dev) if dQ is None else dQ
+    dK = torch.empty((B, H, m, d_k), dtype=torch.bfloat16, device=dev) if dK is None else dK
+    dV = torch.empty((B, H, m, d_v), dtype=torch.bfloat16, device=dev) if dV is None else dV
+    ws_bytes = bwd_workspace_size(B, H, n, m, d_k, d_v)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    elif workspace.numel() < ws_bytes or workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {ws_bytes} bytes")
+    sc = -1.0 if scale is None else float(scale)
+    rc = attn_bwd_raw(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), B, H, n, m, d_k, d_v,
+                      MASK_CODES[mask], _ptr(key_lengths) if uses_lengths else None, sc,
+                      _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace), workspace.numel(),
+                      _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd", last_error() if rc == ATTN_ERR_CUDA else "")
+    return dQ, dK, dV
 
 
 def device_status(stream=None) -> tuple[int, int]:

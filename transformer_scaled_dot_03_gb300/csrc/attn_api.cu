@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -94,6 +95,27 @@ int make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (%d)",
+                 static_cast<int>(r));
+        return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}
+
+// 3-D fp32 map over [bh][rows][d] with a {32, 32, 1} box and 128-byte swizzle
+// (the backward's dQ accumulator, written by TMA reduce-add).
+int make_map_f32(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* base, int64_t bh,
+                 int64_t rows, int64_t d)
+{
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(bh)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d * 4), static_cast<cuuint64_t>(rows * d * 4)};
+    cuuint32_t box[3] = {32u, 32u, 1u};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (f32) failed (%d)",
                  static_cast<int>(r));
         return ATTN_ERR_CUDA;
     }
@@ -360,4 +382,200 @@ extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int
     cudaError_t e = cudaMemsetAsync(scratch, 0, kNoAllocStatusBytes, st);
     if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(no-allocation scratch)", e);
     return launch_attention(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, scale, O, LSE, scratch, st);
+}
+
+// ---------------------------------------------------------------------------
+// Backward.
+namespace {
+
+constexpr size_t kWsAlign = 256;
+constexpr float kLog2e = 1.4426950408889634074f;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace: dQ accumulator fp32 [B*H, n, d_k], then LSE*log2(e) and D, each fp32
+// [B*H, n_pad] with n_pad = n rounded up to whole 128-row query tiles.
+struct BwdWorkspace {
+    size_t lse_off, dd_off, total;
+    int64_t n_pad;
+};
+
+BwdWorkspace bwd_workspace(int64_t bh, int64_t n, int64_t d_k)
+{
+    BwdWorkspace w;
+    w.n_pad = (n + 127) / 128 * 128;
+    const size_t dq = round_up(static_cast<size_t>(bh * n * d_k) * 4, kWsAlign);
+    const size_t row = round_up(static_cast<size_t>(bh * w.n_pad) * 4, kWsAlign);
+    w.lse_off = dq;
+    w.dd_off = dq + row;
+    w.total = dq + 2 * row;
+    return w;
+}
+
+// D_i = sum_c dO_ic O_ic (fp32 from the bf16 tensors) and LSE_i * log2(e) for every
+// row of the padded layout (0 in the padding); zeroes the dQ accumulator. A group of
+// d_v / 8 lanes reads one row, 16 bytes per lane.
+__global__ void bwd_prep_kernel(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
+                                const float* __restrict__ LSE, int64_t bh_count, int n, int64_t n_pad, int d_v,
+                                float* __restrict__ lse2, float* __restrict__ dd, float4* __restrict__ dq_acc,
+                                int64_t dq_vec)
+{
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = tid; i < dq_vec; i += stride) dq_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    const int G = d_v / 8;                       // lanes per row: 8 or 16
+    const int lane = threadIdx.x % 32;
+    const int g = lane % G;
+    const int rows_per_warp = 32 / G;
+    const int64_t total = bh_count * n_pad;
+    const int64_t warp_id = tid / 32;
+    const int64_t warp_stride = stride / 32;
+    for (int64_t r0 = warp_id * rows_per_warp; r0 < total; r0 += warp_stride * rows_per_warp) {
+        const int64_t row = r0 + lane / G;
+        const int64_t bh = row / n_pad;
+        const int64_t q = row - bh * n_pad;
+        const bool valid = row < total && q < n;
+        float acc = 0.f;
+        if (valid) {
+            const int64_t e0 = (bh * n + q) * d_v + 8 * g;
+            const uint4 a = *reinterpret_cast<const uint4*>(O + e0);
+            const uint4 b = *reinterpret_cast<const uint4*>(dO + e0);
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc = fmaf(__uint_as_float(av[k] << 16), __uint_as_float(bv[k] << 16), acc);
+                acc = fmaf(__uint_as_float(av[k] & 0xFFFF0000u), __uint_as_float(bv[k] & 0xFFFF0000u), acc);
+            }
+        }
+        for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (g == 0 && row < total) {
+            dd[row] = valid ? acc : 0.f;
+            lse2[row] = valid ? LSE[bh * n + q] * kLog2e : 0.f;
+        }
+    }
+}
+
+// dQ = bf16(scale * accumulator), four elements per step.
+__global__ void bwd_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dQ, int64_t vec, float scale)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < vec; i += stride) {
+        const float4 a = acc[i];
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+        uint2 o;
+        o.x = *reinterpret_cast<const uint32_t*>(&lo);
+        o.y = *reinterpret_cast<const uint32_t*>(&hi);
+        dQ[i] = o;
+    }
+}
+
+int64_t grid_for(int64_t work, int64_t per_block)
+{
+    return std::max<int64_t>(1, std::min<int64_t>((work + per_block - 1) / per_block, 152 * 8));
+}
+
+}  // namespace
+
+extern "C" size_t attn_bwd_workspace_size(int B, int H, int n, int m, int d_k, int d_v)
+{
+    (void)m;
+    (void)d_v;
+    if (B <= 0 || H <= 0 || n <= 0 || d_k <= 0) return 0;
+    return bwd_workspace(static_cast<int64_t>(B) * H, n, d_k).total;
+}
+
+extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                        const float* LSE, int B, int H, int n, int m, int d_k, int d_v, int mask_kind,
+                        const int32_t* key_lengths, float scale, void* dQ, void* dK, void* dV, void* workspace,
+                        size_t workspace_bytes, void* stream)
+{
+    if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
+    if (attn::mask_has_lengths(mask_kind) && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_ok(d_k) || d_v != d_k) return ATTN_ERR_UNSUPPORTED;
+    if (n > kMaxSeq || m > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0) return ATTN_OK;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    if (bh > INT32_MAX || bh * ((static_cast<int64_t>(m) + 127) / 128) > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool have_rows = n > 0, have_keys = m > 0;
+    if ((have_rows && dQ == nullptr) || (have_keys && (dK == nullptr || dV == nullptr))) return ATTN_ERR_INVALID_ARG;
+    if ((dQ && !aligned(dQ, 16)) || (dK && !aligned(dK, 16)) || (dV && !aligned(dV, 16)))
+        return ATTN_ERR_MISALIGNED;
+    if (!have_rows || !have_keys) {
+        // no queries: dK = dV = 0; no keys: O = 0 is constant, dQ = 0
+        cudaError_t e = cudaSuccess;
+        if (!have_rows) {
+            e = cudaMemsetAsync(dK, 0, static_cast<size_t>(bh) * m * d_k * 2, st);
+            if (e == cudaSuccess) e = cudaMemsetAsync(dV, 0, static_cast<size_t>(bh) * m * d_v * 2, st);
+        } else {
+            e = cudaMemsetAsync(dQ, 0, static_cast<size_t>(bh) * n * d_k * 2, st);
+        }
+        return e == cudaSuccess ? ATTN_OK : fail_cuda("cudaMemsetAsync(empty gradient)", e);
+    }
+    if (Q == nullptr || K == nullptr || V == nullptr || O == nullptr || dO == nullptr || LSE == nullptr ||
+        workspace == nullptr)
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(dO, 16) ||
+        !aligned(LSE, 4) || !aligned(workspace, kWsAlign) || (key_lengths != nullptr && !aligned(key_lengths, 4)))
+        return ATTN_ERR_MISALIGNED;
+    const BwdWorkspace ws = bwd_workspace(bh, n, d_k);
+    if (workspace_bytes < ws.total) return ATTN_ERR_INVALID_ARG;
+
+    uint32_t* status = nullptr;
+    int rc = status_word(&status);
+    if (rc != ATTN_OK) return rc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    if ((rc = encoder(&enc)) != ATTN_OK) return rc;
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    float* dq_acc = reinterpret_cast<float*>(wsb);
+    float* lse2 = reinterpret_cast<float*>(wsb + ws.lse_off);
+    float* dd = reinterpret_cast<float*>(wsb + ws.dd_off);
+
+    attn::BwdMaps maps;
+    if ((rc = make_map(enc, &maps.q, Q, bh, n, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.k, K, bh, m, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.v, V, bh, m, d_v, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.dout, dO, bh, n, d_v, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.dk, dK, bh, m, d_k, 32)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.dv, dV, bh, m, d_v, 32)) != ATTN_OK) return rc;
+    if ((rc = make_map_f32(enc, &maps.dq_acc, dq_acc, bh, n, d_k)) != ATTN_OK) return rc;
+
+    const double sc = (scale > 0.f && std::isfinite(scale)) ? static_cast<double>(scale)
+                                                             : 1.0 / std::sqrt(static_cast<double>(d_k));
+    attn::BwdParams p;
+    p.B = B;
+    p.H = H;
+    p.n = n;
+    p.m = m;
+    p.causal_off = m - n;
+    p.num_kblocks = static_cast<int>((static_cast<int64_t>(m) + 127) / 128);
+    p.n_pad = static_cast<int>(ws.n_pad);
+    p.key_lengths = attn::mask_has_lengths(mask_kind) ? key_lengths : nullptr;
+    p.lse2 = lse2;
+    p.dd = dd;
+    p.dK = dK;
+    p.dV = dV;
+    p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
+    p.scale = static_cast<float>(sc);
+    p.status = status;
+    p.watchdog_ns = g_watchdog_ns;
+    p.debug_flags = g_debug_flags;
+
+    const int64_t dq_vec = bh * n * d_k / 4;
+    const int64_t prep_threads = std::max<int64_t>(dq_vec, bh * ws.n_pad * (d_v / 8));
+    bwd_prep_kernel<<<static_cast<unsigned>(grid_for(prep_threads, 256)), 256, 0, st>>>(
+        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), LSE, bh, n, ws.n_pad, d_v, lse2, dd,
+        reinterpret_cast<float4*>(dq_acc), dq_vec);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda("backward preparation kernel launch", e);
+    e = d_k == 64 ? attn::launch_bwd_d64(mask_kind, maps, p, st) : attn::launch_bwd_d128(mask_kind, maps, p, st);
+    if (e != cudaSuccess) return fail_cuda("backward kernel launch", e);
+    bwd_convert_kernel<<<static_cast<unsigned>(grid_for(dq_vec, 256)), 256, 0, st>>>(
+        reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dQ), dq_vec, p.scale);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? ATTN_OK : fail_cuda("dQ conversion kernel launch", e);
 }

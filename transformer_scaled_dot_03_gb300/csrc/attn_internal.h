@@ -55,6 +55,31 @@ enum { KERNEL_DP = 0, KERNEL_NT1 = 1, KERNEL_NT2 = 2 };
 
 inline int kernel_rows_per_cta(int variant) { return variant == KERNEL_NT2 ? 256 : 128; }
 
+// Backward (attn_kernel_bwd.cuh): one CTA per (b, h, 128-key tile).
+struct BwdParams {
+    int B, H, n, m;
+    int causal_off;               // m - n
+    int num_kblocks;              // ceil(m / 128)
+    int n_pad;                    // query rows padded to whole tiles (lse2 / dd row stride)
+    const int32_t* key_lengths;   // device int32 [B] (key-padding masks only)
+    const float* lse2;            // [B*H, n_pad]: LSE * log2(e), 0 in the padding
+    const float* dd;              // [B*H, n_pad]: D = rowsum(dO * O), 0 in the padding
+    void* dK;                     // bf16 [B,H,m,d] (plain stores for key tiles no query sees)
+    void* dV;
+    float scale_log2;             // scale * log2(e)
+    float scale;
+    uint32_t* status;
+    uint64_t watchdog_ns;
+    uint32_t debug_flags;
+};
+
+struct BwdMaps {
+    CUtensorMap q, k, v, dout, dk, dv, dq_acc;
+};
+
+cudaError_t launch_bwd_d64(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_d128(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+
 // num_ctas: grid of the one-unit-per-CTA variants; num_sms sizes the persistent grid.
 // The NT variants take d_k = d_v, masks none / causal (n = m) / key padding.
 cudaError_t launch_fwd_d64(int mask, int variant, const TensorMaps& maps, const FwdParams& p,

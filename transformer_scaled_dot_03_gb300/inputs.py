@@ -154,6 +154,13 @@ def _lengths(g, B, m, mask, len_lo, len_hi, key_lengths):
     return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
 
 
+def make_grad_output(B, H, n, d_v, seed, value_scale=1.0) -> torch.Tensor:
+    """Upstream gradient dO [B,H,n,d_v] for the backward: i.i.d. N(0,1)*value_scale,
+    rounded to bf16, from its own seeded generator."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    return _normal(g, (B, H, n, d_v), value_scale)
+
+
 def make_projection_inputs(B, H, n, d_model, mask, seed, len_lo, len_hi) -> Inputs:
     """Base-encoder recipe: X ~ N(0,1) [B,n,d_model]; W_Q, W_K, W_V Xavier-uniform
     [d_model, d_model] with bound sqrt(6/(2*d_model)), no bias ("Transformer 详解"
