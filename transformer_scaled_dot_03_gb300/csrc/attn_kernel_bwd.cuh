@@ -179,8 +179,6 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     const uint32_t sQ = sbase + L::Q_OFF;
     const uint32_t sdO = sbase + L::DO_OFF;
     const uint32_t sdS = sbase + L::DS_OFF;
-    const float* s_lse = reinterpret_cast<const float*>(smem + L::LSE_OFF);
-    const float* s_dd = reinterpret_cast<const float*>(smem + L::DD_OFF);
 
     if (warp >= 4) {
         if (warp == L::WARP_TMA && lane == 0) {
@@ -312,48 +310,64 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             if (!ok) break;
             tc_fence_after();
             wait_stores_read();   // this warp's staging rows (the dS rows it writes) are free again
-            const float* lse = s_lse + s * BM;
-            const float* dd = s_dd + s * BM;
-#pragma unroll 1
+            const uint32_t lse_s = sbase + L::LSE_OFF + s * BM * 4;
+            const uint32_t dd_s = sbase + L::DD_OFF + s * BM * 4;
+            const bool need_mask = __any_sync(0xffffffffu, key >= kv_len || q0 + BM - 1 >= p.n ||
+                                                               (mask_is_causal(MASK) && key > q0 + p.causal_off));
+            // Pᵀ: the whole row of Sᵀ (this key against the tile's 128 queries) at once
+            uint32_t sr[BM];
+            tmem_ld32(tmem + lane_base + L::S_COL + 0, sr + 0);
+            tmem_ld32(tmem + lane_base + L::S_COL + 32, sr + 32);
+            tmem_ld32(tmem + lane_base + L::S_COL + 64, sr + 64);
+            tmem_ld32(tmem + lane_base + L::S_COL + 96, sr + 96);
+            tmem_wait_ld();
+#pragma unroll
             for (int c = 0; c < BM / 32; ++c) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tmem + lane_base + L::S_COL + 32 * c, sr);
-                tmem_ld32(tmem + lane_base + L::DP_COL + 32 * c, dr);
-                tmem_wait_ld();
-                const int qc = q0 + 32 * c;              // first query row of this chunk
-                const bool need_mask = __any_sync(
-                    0xffffffffu, key >= kv_len || qc + 31 >= p.n ||
-                                     (mask_is_causal(MASK) && key > qc + p.causal_off));
-                uint32_t pk[16], dk[16];
+                float lz[32];
 #pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(lse + 32 * c + 4 * v);
-                    const float4 d4 = *reinterpret_cast<const float4*>(dd + 32 * c + 4 * v);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pe[4], de[4];
+                for (int v = 0; v < 8; ++v) lds_v4f(lse_s + (32 * c + 4 * v) * 4, lz + 4 * v);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = 4 * v + e;
-                        float pv = ex2_approx(fmaf(__uint_as_float(sr[i]), sl2, -lv[e]));
-                        if (need_mask) {
-                            const int q = qc + i;
-                            const bool vis = key < kv_len && q < p.n &&
-                                             (!mask_is_causal(MASK) || key <= q + p.causal_off);
-                            pv = vis ? pv : 0.f;
-                        }
-                        pe[e] = pv;
-                        de[e] = pv * (__uint_as_float(dr[i]) - dv[e]);
-                    }
-                    pk[2 * v] = pack_bf16x2(pe[0], pe[1]);
-                    pk[2 * v + 1] = pack_bf16x2(pe[2], pe[3]);
-                    dk[2 * v] = pack_bf16x2(de[0], de[1]);
-                    dk[2 * v + 1] = pack_bf16x2(de[2], de[3]);
+                for (int i = 0; i < 32; ++i) {
+                    const int j = 32 * c + i;
+                    sr[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, -lz[i])));
                 }
-                // Pᵀ and dSᵀ over the columns of Sᵀ and dPᵀ already read (chunks <= c)
-                tmem_st16(tmem + lane_base + L::P_COL + 16 * c, pk);
+            }
+            if (need_mask) {
+                // this key is visible to the tile's query columns j in [j_lo, j_hi)
+                const int q_first = key >= kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - p.causal_off : 0);
+                const int j_lo = q_first == INT32_MAX ? BM : max(q_first - q0, 0);
+                const int j_hi = min(p.n - q0, BM);
+#pragma unroll
+                for (int j = 0; j < BM; ++j)
+                    if (j < j_lo || j >= j_hi) sr[j] = 0u;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(sr[64 * h + 2 * i]), __uint_as_float(sr[64 * h + 2 * i + 1]));
+                tmem_st32(tmem + lane_base + L::P_COL + 32 * h, pk);   // over Sᵀ, already read
+            }
+            // dSᵀ = Pᵀ ∘ (dPᵀ - D), 32 queries at a time; dSᵀ goes over the dPᵀ columns
+            // already read and, MN-major (row = key, 64-query chunks), into shared memory
+#pragma unroll
+            for (int c = 0; c < BM / 32; ++c) {
+                uint32_t dr[32];
+                float dz[32];
+                tmem_ld32(tmem + lane_base + L::DP_COL + 32 * c, dr);
+#pragma unroll
+                for (int v = 0; v < 8; ++v) lds_v4f(dd_s + (32 * c + 4 * v) * 4, dz + 4 * v);
+                tmem_wait_ld();
+                uint32_t dk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a = __uint_as_float(sr[32 * c + 2 * i]) * (__uint_as_float(dr[2 * i]) - dz[2 * i]);
+                    const float b =
+                        __uint_as_float(sr[32 * c + 2 * i + 1]) * (__uint_as_float(dr[2 * i + 1]) - dz[2 * i + 1]);
+                    dk[i] = pack_bf16x2(a, b);
+                }
                 tmem_st16(tmem + lane_base + L::DS_COL + 16 * c, dk);
-                // dS, MN-major: row = key r, 64-query chunks; this chunk is 4 pieces of 8 queries
                 const uint32_t row_base = sdS + (c / 2) * CHUNK_BYTES + r * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {

@@ -454,11 +454,11 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 const bool need_mask = __any_sync(
                     0xffffffffu, (key0 + BN > w.kv_len) || (mask_is_causal(MASK) && key0 + BN - 1 > qlim));
                 if (need_mask) {
+                    // this row sees the tile's columns c < c_hi
+                    const int c_hi = (mask_is_causal(MASK) ? min(w.kv_len, qlim + 1) : w.kv_len) - key0;
 #pragma unroll
-                    for (int c = 0; c < BN; ++c) {
-                        const int key = key0 + c;
-                        if (key >= w.kv_len || (mask_is_causal(MASK) && key > qlim)) s[c] = -INFINITY;
-                    }
+                    for (int c = 0; c < BN; ++c)
+                        if (c >= c_hi) s[c] = -INFINITY;
                 }
                 // row maximum: eight independent chains of three-input max
                 float mx[8];

@@ -162,6 +162,15 @@ __device__ __forceinline__ void bulk_wait_group0()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Four consecutive floats from shared memory (16-byte aligned address). Volatile,
+// so it stays after the barrier wait that made the data visible.
+__device__ __forceinline__ void lds_v4f(uint32_t addr, float* v)
+{
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+                 : "r"(addr));
+}
+
 // Order this thread's generic-proxy shared-memory writes before later async-proxy reads.
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
