@@ -190,11 +190,21 @@ def run_ours(args):
             sets.append((x.Q.to(dev), x.K.to(dev), x.V.to(dev),
                          torch.empty(w.B, w.H, w.n, w.d_v, dtype=torch.bfloat16, device=dev),
                          torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)))
+    decode = w.path == "decode"
+    ws_bytes = attn.decode_workspace_size(w.B, w.H, w.n, w.m, w.d_k, w.d_v) if decode else 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+    launches_per_step = 2 if ws_bytes else 1        # the few-row pass merges its key chunks
     torch.cuda.synchronize(dev)
+
+    def run(Q, K, V, lens, O, L):
+        if decode:
+            attn.attn_decode(Q, K, V, w.mask, lens, x.scale, O=O, LSE=L, workspace=ws, stream=stream)
+        else:
+            attn.attn_fwd(Q, K, V, w.mask, lens, x.scale, O=O, LSE=L, stream=stream)
 
     def step(i):
         Q, K, V, O, L = sets[i % copies]
-        attn.attn_fwd(Q, K, V, w.mask, lens_d, x.scale, O=O, LSE=L, stream=stream)
+        run(Q, K, V, lens_d, O, L)
 
     # warm-up (also creates the status word before any graph capture)
     for i in range(args.warmup):
@@ -253,7 +263,7 @@ def run_ours(args):
         dV.copy_(hV, non_blocking=True)
         if dlens is not None:
             dlens.copy_(hlens, non_blocking=True)
-        attn.attn_fwd(dQ, dK, dV, w.mask, dlens, x.scale, O=dO, LSE=dL, stream=stream)
+        run(dQ, dK, dV, dlens, dO, dL)
         hO.copy_(dO, non_blocking=True)
         hL.copy_(dL, non_blocking=True)
 
@@ -279,9 +289,26 @@ def run_ours(args):
     e2e_value = job_value(flops, world, e2e_ms)
     peak, peak_sus, hbm, src = peaks()
     kernel_tflops = flops / (ms * 1e-3) / 1e12
-    if kernel_tflops > 1.25 * peak or ms * K_steps < 0.5 * t_wall * 1e3 * 0.5:
+    alg_bytes = w.decode_bytes(x.key_lengths) if decode else in_bytes + out_bytes
+    hbm_gbs = alg_bytes / (ms * 1e-3) / 1e9
+    if kernel_tflops > 1.25 * peak or hbm_gbs > 1.25 * hbm or ms * K_steps < 0.5 * t_wall * 1e3 * 0.5:
         raise RuntimeError(f"implausible timing: {kernel_tflops:.1f} TFLOP/s, device {ms * K_steps:.2f} ms "
                            f"vs wall {t_wall * 1e3:.2f} ms")
+
+    traffic = args.traffic if args.traffic is not None else measured_traffic(w.name)
+    if decode:
+        roofline = {"bound": "hbm", "achieved": round(hbm_gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(hbm_gbs / hbm, 4), "traffic": traffic,
+                    "traffic_unit": "bytes per launch (ncu dram read+write)",
+                    "peak_source": f"{src} HBM copy",
+                    "algorithmic_bytes": alg_bytes}
+    else:
+        roofline = {"bound": "tensor", "achieved": round(kernel_tflops, 2),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
+                    "traffic": traffic,
+                    "traffic_unit": "bytes per launch (ncu dram read+write)",
+                    "peak_source": f"{src} bf16 burst",
+                    "hbm_gbs_achieved": round(hbm_gbs, 1), "hbm_frac": round(hbm_gbs / hbm, 4)}
 
     result = None
     if rank == 0:
@@ -300,19 +327,13 @@ def run_ours(args):
                        "global_batch": w.B * world, "parallelism": f"replicas{world}",
                        "l2": f"rotating {copies} input/output sets "
                              f"({copies * (in_bytes + out_bytes) / 2**20:.0f} MiB > 2x L2)",
-                       "timing": f"CUDA graph of {G} launches x {reps} replays between events"},
+                       "timing": f"CUDA graph of {G} steps x {reps} replays between events"},
             "pct_of_peak": round(100.0 * value / world / peak, 2),
             "effective_tflops": round(world * eff_flops / (ms * 1e-3) / 1e12, 2),
-            "roofline": {"bound": "tensor", "achieved": round(kernel_tflops, 2),
-                         "peak": peak, "unit": "TFLOP/s", "frac": round(kernel_tflops / peak, 4),
-                         "traffic": args.traffic if args.traffic is not None else measured_traffic(w.name),
-                         "traffic_unit": "bytes per launch (ncu dram read+write)",
-                         "peak_source": f"{src} bf16 burst",
-                         "hbm_gbs_achieved": round((in_bytes + out_bytes) / (ms * 1e-3) / 1e9, 1),
-                         "hbm_frac": round((in_bytes + out_bytes) / (ms * 1e-3) / 1e9 / hbm, 4)},
+            "roofline": roofline,
             "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-            "gpu_launches": K_steps,
+            "gpu_launches": K_steps * launches_per_step,
             "clocks": clocks,
             "wall_s_timed": round(t_wall, 3),
         }
@@ -413,7 +434,7 @@ def main():
     ap.add_argument("--steps", type=int, default=65536)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER + inputs.VARIANT_ORDER)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER + inputs.VARIANT_ORDER + inputs.DECODE_ORDER)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -179,6 +179,33 @@ int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const v
              const int32_t* key_lengths, float scale, void* dQ, void* dK, void* dV,
              void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Attention forward for a few query rows against a long key/value sequence:
+ * the decoding step of a model that keeps its keys and values in a cache
+ * (each new token's query attends to every cached position). Same operation,
+ * masks, layouts and results as attn_fwd (any n <= 8 gives the same O and LSE
+ * up to rounding); the implementation streams K and V once from memory with a
+ * split over the keys instead of the tensor-core tiles of attn_fwd, which pays
+ * off when n is small.
+ *   n            1..8 query rows per (b, h); 0 is a no-op; more is
+ *                ATTN_ERR_UNSUPPORTED (use attn_fwd).
+ *   d_k, d_v     equal, 64 or 128.
+ *   key_lengths  for the key-padding masks: the valid cache length per batch
+ *                entry (as in attn_fwd).
+ *   workspace    device scratch for the per-chunk partial results, owned by the
+ *                caller, 256-byte aligned, at least
+ *                attn_decode_workspace_size(...) bytes (0 when the keys of a
+ *                (b, h) pair are not split; the pointer may then be NULL).
+ * Kernels on `stream`: the split kernel, then (if the keys were split) a merge
+ * kernel. Returns ATTN_OK or a negative attn_status_t; on error nothing is
+ * enqueued.
+ */
+size_t attn_decode_workspace_size(int B, int H, int n, int m, int d_k, int d_v);
+
+int attn_decode(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+                int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
+                void* workspace, size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status code. */
 const char* attn_status_string(int status);
 

@@ -141,3 +141,35 @@ def test_bwd_workspace_size():
 @pytest.mark.parametrize("kw", [dict(B=0), dict(H=0)])
 def test_bwd_empty_problem_is_a_noop(lib, kw):
     assert call_bwd(**kw) == attn.ATTN_OK
+
+
+def call_dec(B=1, H=1, n=1, m=4096, dk=64, dv=64, mask=0, lens=None, O=P2, ws=P, ws_bytes=1 << 24):
+    return attn.attn_decode_raw(P, P, P, B, H, n, m, dk, dv, mask, lens, -1.0, O, None, ws, ws_bytes, 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(n=9), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dk=64, dv=128), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dk=32, dv=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(mask=2, lens=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(O=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ws=None), attn.ATTN_ERR_INVALID_ARG),          # this size splits the keys
+    (dict(ws_bytes=64), attn.ATTN_ERR_INVALID_ARG),
+    (dict(ws=ctypes.c_void_p(0x10040)), attn.ATTN_ERR_MISALIGNED),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code):
+    assert call_dec(**kw) == code
+
+
+def test_decode_workspace_size():
+    # one (b, h) pair with 4096 keys: split into 16 chunks of 256 keys
+    assert attn.decode_workspace_size(1, 1, 1, 4096, 64, 64) == 16 * 64 * 4 + 256
+    # 640 or more (b, h) pairs: no split, no workspace
+    assert attn.decode_workspace_size(40, 16, 1, 4096, 128, 128) == 0
+    assert attn.decode_workspace_size(0, 16, 1, 4096, 128, 128) == 0
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(n=0)])
+def test_decode_empty_is_noop(lib, kw):
+    assert call_dec(**kw) == attn.ATTN_OK

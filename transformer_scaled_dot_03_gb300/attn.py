@@ -33,7 +33,8 @@ MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PAD
 
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
-           "attn_last_error", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size")
+           "attn_last_error", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
+           "attn_decode_workspace_size")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +70,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_bwd.restype = i32
         lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.attn_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp,
+                                    ctypes.c_size_t, vp]
+        lib.attn_decode.restype = i32
+        lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_decode_workspace_size.restype = ctypes.c_size_t
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         _lib = lib
@@ -194,6 +200,60 @@ def attn_bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor,
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd", last_error() if rc == ATTN_ERR_CUDA else "")
     return dQ, dK, dV
+
+
+def decode_workspace_size(B, H, n, m, d_k, d_v) -> int:
+    return int(load().attn_decode_workspace_size(int(B), int(H), int(n), int(m), int(d_k), int(d_v)))
+
+
+def attn_decode_raw(Q_ptr, K_ptr, V_ptr, B, H, n, m, d_k, d_v, mask_kind, key_lengths_ptr, scale, O_ptr,
+                    LSE_ptr, ws_ptr, ws_bytes, stream_handle) -> int:
+    """The C decode entry point with plain integers/pointers; returns the status code."""
+    return load().attn_decode(Q_ptr, K_ptr, V_ptr, int(B), int(H), int(n), int(m), int(d_k), int(d_v),
+                              int(mask_kind), key_lengths_ptr, ctypes.c_float(scale), O_ptr, LSE_ptr, ws_ptr,
+                              ctypes.c_size_t(ws_bytes), ctypes.c_void_p(stream_handle))
+
+
+def attn_decode(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "none",
+                key_lengths: torch.Tensor | None = None, scale: float | None = None,
+                O: torch.Tensor | None = None, LSE: torch.Tensor | None = None, want_lse: bool = True,
+                workspace: torch.Tensor | None = None, stream=None):
+    """Few-row attention forward (n <= 8 query rows per head against m keys, e.g. one
+    decoding step against a key/value cache): same arguments and results as
+    ``attn_fwd``. ``workspace`` (uint8 CUDA tensor of at least ``decode_workspace_size``
+    bytes) is allocated here when omitted and needed."""
+    if mask not in MASK_CODES:
+        raise ValueError(f"unknown mask {mask!r}")
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    B, H, n, d_k = Q.shape
+    m = K.shape[2]
+    d_v = V.shape[3]
+    if tuple(K.shape) != (B, H, m, d_k) or tuple(V.shape[:3]) != (B, H, m):
+        raise ValueError("inconsistent Q/K/V shapes")
+    uses_lengths = mask in _inputs.LENGTH_MASKS
+    if uses_lengths and (key_lengths is None or key_lengths.dtype != torch.int32
+                         or not key_lengths.is_cuda or key_lengths.numel() != B
+                         or not key_lengths.is_contiguous()):
+        raise ValueError(f"{mask} needs key_lengths: contiguous int32 CUDA [B]")
+    if O is None:
+        O = torch.empty((B, H, n, d_v), dtype=torch.bfloat16, device=Q.device)
+    if LSE is None and want_lse:
+        LSE = torch.empty((B, H, n), dtype=torch.float32, device=Q.device)
+    ws_bytes = decode_workspace_size(B, H, n, m, d_k, d_v)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=Q.device)
+    if workspace is not None and (workspace.numel() < ws_bytes or workspace.dtype != torch.uint8):
+        raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {ws_bytes} bytes")
+    sc = -1.0 if scale is None else float(scale)
+    rc = attn_decode_raw(_ptr(Q), _ptr(K), _ptr(V), B, H, n, m, d_k, d_v, MASK_CODES[mask],
+                         _ptr(key_lengths) if uses_lengths else None, sc, _ptr(O), _ptr(LSE),
+                         _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                         _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode", last_error() if rc == ATTN_ERR_CUDA else "")
+    return O, LSE
 
 
 def device_status(stream=None) -> tuple[int, int]:

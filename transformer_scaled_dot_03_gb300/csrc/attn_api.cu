@@ -579,3 +579,98 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
     e = cudaGetLastError();
     return e == cudaSuccess ? ATTN_OK : fail_cuda("dQ conversion kernel launch", e);
 }
+
+// ---------------------------------------------------------------------------
+// Few-row forward (decoding against a key/value cache).
+namespace {
+
+constexpr int kDecodeMaxRows = 8;
+constexpr int64_t kDecodeTargetCtas = 640;   // a few waves of CTAs on a 148-160 SM part
+
+// Keys per chunk (a multiple of 128, at least 256) and the number of chunks:
+// enough chunks that B*H*chunks reaches the CTA target. Independent of the device
+// so that the workspace size can be computed without one.
+void decode_split(int64_t bh, int m, int* split_len, int* num_splits)
+{
+    const int64_t max_splits = std::max<int64_t>(1, (m + 255) / 256);
+    int64_t s = std::min<int64_t>(std::max<int64_t>(1, (kDecodeTargetCtas + bh - 1) / bh), max_splits);
+    int64_t len = ((m + s - 1) / s + 127) / 128 * 128;
+    s = (m + len - 1) / len;
+    *split_len = static_cast<int>(len);
+    *num_splits = static_cast<int>(std::max<int64_t>(s, 1));
+}
+
+int decode_rows(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
+
+}  // namespace
+
+extern "C" size_t attn_decode_workspace_size(int B, int H, int n, int m, int d_k, int d_v)
+{
+    (void)d_v;
+    if (B <= 0 || H <= 0 || n <= 0 || m <= 0 || d_k <= 0) return 0;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    int split_len = 0, num_splits = 0;
+    decode_split(bh, m, &split_len, &num_splits);
+    if (num_splits == 1) return 0;
+    const size_t rows = static_cast<size_t>(bh) * num_splits * n;
+    return round_up(rows * d_k * 4, kWsAlign) + round_up(rows * 2 * 4, kWsAlign);
+}
+
+extern "C" int attn_decode(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+                           int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
+                           void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
+    if (attn::mask_has_lengths(mask_kind) && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_ok(d_k) || d_v != d_k || n > kDecodeMaxRows) return ATTN_ERR_UNSUPPORTED;
+    if (m > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
+    if (B == 0 || H == 0 || n == 0) return ATTN_OK;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    if (O == nullptr || (m > 0 && (Q == nullptr || K == nullptr || V == nullptr))) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(O, 16) || !aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16)) return ATTN_ERR_MISALIGNED;
+    if ((LSE != nullptr && !aligned(LSE, 4)) || (key_lengths != nullptr && !aligned(key_lengths, 4)))
+        return ATTN_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (m == 0) return fill_no_keys(bh, n, d_v, O, LSE, st);
+    int split_len = 0, num_splits = 0;
+    decode_split(bh, m, &split_len, &num_splits);
+    if (bh * num_splits > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_decode_workspace_size(B, H, n, m, d_k, d_v);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
+    if (need > 0 && !aligned(workspace, kWsAlign)) return ATTN_ERR_MISALIGNED;
+
+    uint32_t* status = nullptr;
+    int rc = status_word(&status);
+    if (rc != ATTN_OK) return rc;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    if ((rc = encoder(&enc)) != ATTN_OK) return rc;
+    CUtensorMap tmK, tmV;
+    if ((rc = make_map(enc, &tmK, K, bh, m, d_k, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &tmV, V, bh, m, d_v, 128)) != ATTN_OK) return rc;
+
+    const double sc = (scale > 0.f && std::isfinite(scale)) ? static_cast<double>(scale)
+                                                             : 1.0 / std::sqrt(static_cast<double>(d_k));
+    attn::DecodeParams p;
+    p.Q = static_cast<const uint16_t*>(Q);
+    p.B = B;
+    p.H = H;
+    p.n = n;
+    p.m = m;
+    p.causal_off = m - n;
+    p.mask = mask_kind;
+    p.key_lengths = attn::mask_has_lengths(mask_kind) ? key_lengths : nullptr;
+    p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
+    p.split_len = split_len;
+    p.num_splits = num_splits;
+    p.O = static_cast<uint16_t*>(O);
+    p.LSE = LSE;
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    const size_t prow = static_cast<size_t>(bh) * num_splits * n;
+    p.part_o = need > 0 ? reinterpret_cast<float*>(wsb) : nullptr;
+    p.part_ml = need > 0 ? reinterpret_cast<float*>(wsb + round_up(prow * d_k * 4, kWsAlign)) : nullptr;
+    p.status = status;
+    p.watchdog_ns = g_watchdog_ns;
+    cudaError_t e = attn::launch_decode(d_k, decode_rows(n), tmK, tmV, p, st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda("decode kernel launch", e);
+}

@@ -1,0 +1,27 @@
+// attn_decode.cu -- instantiations of the few-row (decoding) forward kernel.
+#include "attn_kernel_decode.cuh"
+
+namespace attn {
+
+template <int D>
+static cudaError_t launch_rows(int rows, const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p,
+                               cudaStream_t stream)
+{
+    switch (rows) {
+    case 1: return dec::launch<D, 1>(tmK, tmV, p, stream);
+    case 2: return dec::launch<D, 2>(tmK, tmV, p, stream);
+    case 4: return dec::launch<D, 4>(tmK, tmV, p, stream);
+    case 8: return dec::launch<D, 8>(tmK, tmV, p, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decode(int d, int rows, const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p,
+                          cudaStream_t stream)
+{
+    if (d == 64) return launch_rows<64>(rows, tmK, tmV, p, stream);
+    if (d == 128) return launch_rows<128>(rows, tmK, tmV, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

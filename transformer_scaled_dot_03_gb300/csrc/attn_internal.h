@@ -80,6 +80,28 @@ struct BwdMaps {
 cudaError_t launch_bwd_d64(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_d128(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 
+// Few-row forward (attn_kernel_decode.cuh): one CTA per (b, h, key chunk).
+struct DecodeParams {
+    const uint16_t* Q;            // bf16 [B,H,n,d]
+    int B, H, n, m;
+    int causal_off;               // m - n
+    int mask;
+    const int32_t* key_lengths;   // device int32 [B] (key-padding masks only)
+    float scale_log2;             // scale * log2(e)
+    int split_len;                // keys per chunk (multiple of 128)
+    int num_splits;               // chunks per (b, h)
+    uint16_t* O;                  // bf16 [B,H,n,d]
+    float* LSE;                   // fp32 [B,H,n] or null
+    float* part_o;                // fp32 [B*H, num_splits, n, d] (num_splits > 1)
+    float* part_ml;               // fp32 [B*H, num_splits, n, 2]: max (log2 domain), sum
+    uint32_t* status;
+    uint64_t watchdog_ns;
+};
+
+// rows: the kernel variant handles n <= rows (1, 2, 4 or 8).
+cudaError_t launch_decode(int d, int rows, const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p,
+                          cudaStream_t stream);
+
 // num_ctas: grid of the one-unit-per-CTA variants; num_sms sizes the persistent grid.
 // The NT variants take d_k = d_v, masks none / causal (n = m) / key padding.
 cudaError_t launch_fwd_d64(int mask, int variant, const TensorMaps& maps, const FwdParams& p,

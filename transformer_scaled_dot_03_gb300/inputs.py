@@ -61,11 +61,22 @@ class Workload:
     len_lo: int = 0                 # key-padding valid length range, inclusive
     len_hi: int = 0
     d_model: int = 0                # projection recipe only
+    path: str = "fwd"               # "fwd": attn_fwd; "decode": the few-row attn_decode
 
     def flops(self) -> float:
         """Nominal forward FLOPs: 2*d_k (scores) + 2*d_v (weighted sum) per visible
         (query, key) pair (``nominal_pairs``; half of n*m for a square causal mask)."""
         return 2.0 * self.B * self.H * (self.d_k + self.d_v) * nominal_pairs(self.n, self.m, self.mask)
+
+    def decode_bytes(self, key_lengths=None) -> float:
+        """Algorithmic HBM bytes of a few-row pass: the visible K and V rows once (per
+        batch entry min(length, m) rows under the key-padding masks), Q, O and LSE."""
+        if key_lengths is not None and self.mask in LENGTH_MASKS:
+            rows = float(key_lengths.clamp(0, self.m).sum()) * self.H
+        else:
+            rows = float(self.B) * self.H * self.m
+        bh = self.B * self.H
+        return rows * 2 * (self.d_k + self.d_v) + bh * self.n * (2 * self.d_k + 2 * self.d_v + 4)
 
     def io_bytes(self) -> int:
         """Algorithmic HBM bytes: Q, K, V read once (bf16); O (bf16) and LSE (fp32) written once."""
@@ -105,6 +116,17 @@ WORKLOADS.update({
     "wide_values": Workload("wide_values", 16, 16, 1024, 1024, 64, 128, MASK_NONE, seed=7),
 })
 VARIANT_ORDER = ["decoder_target_mask", "prefill_continuation", "wide_values"]
+
+# Decoding steps against a key/value cache (the few-row attn_decode): a served batch
+# of 64 sequences x 16 heads with cache lengths in [4096, 8192] of 8192 slots, and
+# one long-context pair of sequences with 32768 cached positions. d 128, one query.
+WORKLOADS.update({
+    "decode_kv_cache": Workload("decode_kv_cache", 64, 16, 1, 8192, 128, 128, MASK_KEY_PADDING, seed=8,
+                                len_lo=4096, len_hi=8192, path="decode"),
+    "decode_long_context": Workload("decode_long_context", 2, 16, 1, 32768, 128, 128, MASK_NONE, seed=9,
+                                    path="decode"),
+})
+DECODE_ORDER = ["decode_kv_cache", "decode_long_context"]
 
 
 @dataclasses.dataclass
