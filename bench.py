@@ -40,6 +40,7 @@ import torch  # noqa: E402
 from transformer_scaled_dot_03_gb300 import inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (bf16) at 1 GB300 and % of dense BF16 tensor peak"
+METRIC_BWD = "attention bwd TFLOP/s (bf16; nominal 2.5x the forward's FLOPs) at 1 GB300"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "base_encoder_keypad"
 L2_BYTES = 129 * 1024 * 1024
@@ -177,34 +178,57 @@ def run_ours(args):
     attn.load()
 
     w, x = make_workload(args.workload)
-    flops = w.flops()
-    eff_flops = effective_flops(w, x)
-    in_bytes = x.Q.numel() * 2 + x.K.numel() * 2 + x.V.numel() * 2
-    out_bytes = w.B * w.H * w.n * (w.d_v * 2 + 4)
+    bwd = args.pass_ == "bwd"
+    decode = w.path == "decode" and not bwd
+    # the backward's five products against the forward's two: 2.5x the nominal FLOPs
+    flops = w.flops() * (2.5 if bwd else 1.0)
+    eff_flops = effective_flops(w, x) * (2.5 if bwd else 1.0)
+    qkv_bytes = x.Q.numel() * 2 + x.K.numel() * 2 + x.V.numel() * 2
+    o_bytes = w.B * w.H * w.n * (w.d_v * 2 + 4)
+    if bwd:
+        # inputs Q, K, V, O, LSE, dO; outputs dQ, dK, dV
+        in_bytes = qkv_bytes + o_bytes + w.B * w.H * w.n * w.d_v * 2
+        out_bytes = qkv_bytes
+    else:
+        in_bytes, out_bytes = qkv_bytes, o_bytes
     copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_bytes)))
     stream = torch.cuda.Stream(device=dev)
     lens_d = x.key_lengths.to(dev) if x.key_lengths is not None else None
+    dO_h = inputs.make_grad_output(w.B, w.H, w.n, w.d_v, seed=100 + w.seed) if bwd else None
     sets = []
     with torch.cuda.stream(stream):
         for _ in range(copies):
-            sets.append((x.Q.to(dev), x.K.to(dev), x.V.to(dev),
-                         torch.empty(w.B, w.H, w.n, w.d_v, dtype=torch.bfloat16, device=dev),
-                         torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)))
-    decode = w.path == "decode"
-    ws_bytes = attn.decode_workspace_size(w.B, w.H, w.n, w.m, w.d_k, w.d_v) if decode else 0
+            st = [x.Q.to(dev), x.K.to(dev), x.V.to(dev),
+                  torch.empty(w.B, w.H, w.n, w.d_v, dtype=torch.bfloat16, device=dev),
+                  torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)]
+            if bwd:
+                attn.attn_fwd(st[0], st[1], st[2], w.mask, lens_d, x.scale, O=st[3], LSE=st[4], stream=stream)
+                st += [dO_h.to(dev), torch.empty_like(st[0]), torch.empty_like(st[1]), torch.empty_like(st[2])]
+            sets.append(tuple(st))
+    if bwd:
+        ws_bytes = attn.bwd_workspace_size(w.B, w.H, w.n, w.m, w.d_k, w.d_v)
+        launches_per_step = 3                        # preparation, main kernel, dQ conversion
+    elif decode:
+        ws_bytes = attn.decode_workspace_size(w.B, w.H, w.n, w.m, w.d_k, w.d_v)
+        launches_per_step = 2 if ws_bytes else 1    # the few-row pass merges its key chunks
+    else:
+        ws_bytes, launches_per_step = 0, 1
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
-    launches_per_step = 2 if ws_bytes else 1        # the few-row pass merges its key chunks
     torch.cuda.synchronize(dev)
 
-    def run(Q, K, V, lens, O, L):
-        if decode:
+    def run(st, lens):
+        if bwd:
+            Q, K, V, O, L, dO, dQ, dK, dV = st
+            attn.attn_bwd(Q, K, V, O, L, dO, w.mask, lens, x.scale, dQ, dK, dV, workspace=ws, stream=stream)
+        elif decode:
+            Q, K, V, O, L = st
             attn.attn_decode(Q, K, V, w.mask, lens, x.scale, O=O, LSE=L, workspace=ws, stream=stream)
         else:
+            Q, K, V, O, L = st
             attn.attn_fwd(Q, K, V, w.mask, lens, x.scale, O=O, LSE=L, stream=stream)
 
     def step(i):
-        Q, K, V, O, L = sets[i % copies]
-        run(Q, K, V, lens_d, O, L)
+        run(sets[i % copies], lens_d)
 
     # warm-up (also creates the status word before any graph capture)
     for i in range(args.warmup):
@@ -248,24 +272,24 @@ def run_ours(args):
     if rc != attn.ATTN_OK:
         raise RuntimeError(f"device status {rc} ({detail}) after the timed region")
 
-    # end to end through the C entry point with pinned host buffers
-    hQ, hK, hV = x.Q.pin_memory(), x.K.pin_memory(), x.V.pin_memory()
+    # end to end through the C entry point with pinned host buffers: every input of
+    # the pass host -> device, the pass, every output device -> host
+    dev_set = sets[0]
+    n_in = 6 if bwd else 3                   # Q, K, V (+ O, LSE, dO for the backward)
+    host_in = [t.cpu().pin_memory() for t in dev_set[:n_in]]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_set[n_in:]]
     hlens = x.key_lengths.pin_memory() if x.key_lengths is not None else None
-    hO = torch.empty(w.B, w.H, w.n, w.d_v, dtype=torch.bfloat16).pin_memory()
-    hL = torch.empty(w.B, w.H, w.n, dtype=torch.float32).pin_memory()
-    dQ, dK, dV, dO, dL = sets[0]
     dlens = torch.empty_like(lens_d) if lens_d is not None else None
     e2e_steps = max(3, min(args.e2e_steps, K_steps))
 
     def e2e_step():
-        dQ.copy_(hQ, non_blocking=True)
-        dK.copy_(hK, non_blocking=True)
-        dV.copy_(hV, non_blocking=True)
+        for h, d in zip(host_in, dev_set[:n_in]):
+            d.copy_(h, non_blocking=True)
         if dlens is not None:
             dlens.copy_(hlens, non_blocking=True)
-        run(dQ, dK, dV, dlens, dO, dL)
-        hO.copy_(dO, non_blocking=True)
-        hL.copy_(dL, non_blocking=True)
+        run(dev_set, dlens)
+        for h, d in zip(host_out, dev_set[n_in:]):
+            h.copy_(d, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -281,8 +305,8 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    h2d = in_bytes + (hlens.numel() * 4 if hlens is not None else 0)
-    d2h = hO.numel() * 2 + hL.numel() * 4
+    h2d = sum(t.numel() * t.element_size() for t in host_in) + (hlens.numel() * 4 if hlens is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
 
     ms, e2e_ms = reduce_over_ranks(dev_ms / K_steps, e2e_ms, world)
     value = job_value(flops, world, ms)
@@ -295,7 +319,9 @@ def run_ours(args):
         raise RuntimeError(f"implausible timing: {kernel_tflops:.1f} TFLOP/s, device {ms * K_steps:.2f} ms "
                            f"vs wall {t_wall * 1e3:.2f} ms")
 
-    traffic = args.traffic if args.traffic is not None else measured_traffic(w.name)
+    # the committed traffic figure belongs to the forward tensor-core kernel
+    traffic = args.traffic if args.traffic is not None else (
+        None if (bwd or decode) else measured_traffic(w.name))
     if decode:
         roofline = {"bound": "hbm", "achieved": round(hbm_gbs, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(hbm_gbs / hbm, 4), "traffic": traffic,
@@ -313,15 +339,16 @@ def run_ours(args):
     result = None
     if rank == 0:
         cpu = None
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and not bwd:
             cpu = cpu_baseline(w, x, args.cpu_seconds)
         clocks = clk.summary()
         result = {
-            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC_BWD if bwd else METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; bias-free Xavier projections of X~N(0,1))",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "n": w.n, "m": w.m,
+            "config": {"workload": w.name, "pass": "bwd" if bwd else ("decode" if decode else "fwd"),
+                       "B": w.B, "H": w.H, "n": w.n, "m": w.m,
                        "d_k": w.d_k, "d_v": w.d_v, "mask": w.mask,
                        "key_lengths": [w.len_lo, w.len_hi] if w.mask in inputs.LENGTH_MASKS else None,
                        "global_batch": w.B * world, "parallelism": f"replicas{world}",
@@ -436,6 +463,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER + inputs.VARIANT_ORDER + inputs.DECODE_ORDER)
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="fwd: the forward (the headline); bwd: the backward of the same workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
