@@ -194,8 +194,11 @@ int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const v
  *                entry (as in attn_fwd).
  *   workspace    device scratch for the per-chunk partial results, owned by the
  *                caller, 256-byte aligned, at least
- *                attn_decode_workspace_size(...) bytes (0 when the keys of a
- *                (b, h) pair are not split; the pointer may then be NULL).
+ *                attn_decode_workspace_size(...) bytes. The size covers the
+ *                largest chunk count any device may use; it is 0 when the keys of
+ *                a (b, h) pair are never split (B*H >= 2048 or m <= 256), and the
+ *                pointer may then be NULL. The chunk count itself is chosen per
+ *                launch from the device's SM count.
  * Kernels on `stream`: the split kernel, then (if the keys were split) a merge
  * kernel. Returns ATTN_OK or a negative attn_status_t; on error nothing is
  * enqueued.

@@ -165,8 +165,10 @@ def test_decode_rejects_bad_arguments(lib, kw, code):
 def test_decode_workspace_size():
     # one (b, h) pair with 4096 keys: split into 16 chunks of 256 keys
     assert attn.decode_workspace_size(1, 1, 1, 4096, 64, 64) == 16 * 64 * 4 + 256
-    # 640 or more (b, h) pairs: no split, no workspace
-    assert attn.decode_workspace_size(40, 16, 1, 4096, 128, 128) == 0
+    # 2048 or more (b, h) pairs: never split, no workspace
+    assert attn.decode_workspace_size(128, 16, 1, 4096, 128, 128) == 0
+    # sized for the largest chunk count a launch may pick: min(ceil(m/256), ceil(2048/(B*H)))
+    assert attn.decode_workspace_size(40, 16, 2, 4096, 128, 128) == 640 * 4 * 2 * 128 * 4 + 640 * 4 * 2 * 8
     assert attn.decode_workspace_size(0, 16, 1, 4096, 128, 128) == 0
 
 

@@ -585,19 +585,40 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
 namespace {
 
 constexpr int kDecodeMaxRows = 8;
-constexpr int64_t kDecodeTargetCtas = 640;   // a few waves of CTAs on a 148-160 SM part
+constexpr int64_t kDecodeMaxCtas = 2048;      // bound on B*H*chunks used to size the workspace
+constexpr int64_t kDecodeCtaOverheadKeys = 256;
 
-// Keys per chunk (a multiple of 128, at least 256) and the number of chunks:
-// enough chunks that B*H*chunks reaches the CTA target. Independent of the device
-// so that the workspace size can be computed without one.
-void decode_split(int64_t bh, int m, int* split_len, int* num_splits)
+// Largest number of key chunks (of at least 256 keys) a launch may use for
+// this shape; independent of the device so that the workspace size can be
+// computed without one.
+int64_t decode_split_cap(int64_t bh, int m)
 {
-    const int64_t max_splits = std::max<int64_t>(1, (m + 255) / 256);
-    int64_t s = std::min<int64_t>(std::max<int64_t>(1, (kDecodeTargetCtas + bh - 1) / bh), max_splits);
-    int64_t len = ((m + s - 1) / s + 127) / 128 * 128;
-    s = (m + len - 1) / len;
+    const int64_t by_keys = std::max<int64_t>(1, (m + 255) / 256);
+    const int64_t by_ctas = std::max<int64_t>(1, (kDecodeMaxCtas + bh - 1) / bh);
+    return std::min(by_keys, by_ctas);
+}
+
+// Chunk count for a launch on `slots` concurrent CTAs (SMs x CTAs per SM): the
+// count in [1, cap] that minimises waves x (keys per CTA + a per-CTA overhead),
+// the smaller one on ties. Chunks are whole 128-key tiles.
+void decode_split(int64_t bh, int m, int64_t slots, int* split_len, int* num_splits)
+{
+    const int64_t cap = decode_split_cap(bh, m);
+    int64_t best_s = 1, best_t = INT64_MAX;
+    for (int64_t s = 1; s <= cap; ++s) {
+        const int64_t len = ((m + s - 1) / s + 127) / 128 * 128;
+        const int64_t used = (m + len - 1) / len;                 // chunks that hold keys
+        if (used != s) continue;
+        const int64_t waves = (bh * s + slots - 1) / slots;
+        const int64_t t = waves * (len + kDecodeCtaOverheadKeys);
+        if (t < best_t) {
+            best_t = t;
+            best_s = s;
+        }
+    }
+    const int64_t len = ((m + best_s - 1) / best_s + 127) / 128 * 128;
     *split_len = static_cast<int>(len);
-    *num_splits = static_cast<int>(std::max<int64_t>(s, 1));
+    *num_splits = static_cast<int>(best_s);
 }
 
 int decode_rows(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
@@ -609,10 +630,9 @@ extern "C" size_t attn_decode_workspace_size(int B, int H, int n, int m, int d_k
     (void)d_v;
     if (B <= 0 || H <= 0 || n <= 0 || m <= 0 || d_k <= 0) return 0;
     const int64_t bh = static_cast<int64_t>(B) * H;
-    int split_len = 0, num_splits = 0;
-    decode_split(bh, m, &split_len, &num_splits);
-    if (num_splits == 1) return 0;
-    const size_t rows = static_cast<size_t>(bh) * num_splits * n;
+    const int64_t cap = decode_split_cap(bh, m);
+    if (cap == 1) return 0;
+    const size_t rows = static_cast<size_t>(bh) * cap * n;
     return round_up(rows * d_k * 4, kWsAlign) + round_up(rows * 2 * 4, kWsAlign);
 }
 
@@ -633,12 +653,15 @@ extern "C" int attn_decode(const void* Q, const void* K, const void* V, int B, i
         return ATTN_ERR_MISALIGNED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (m == 0) return fill_no_keys(bh, n, d_v, O, LSE, st);
-    int split_len = 0, num_splits = 0;
-    decode_split(bh, m, &split_len, &num_splits);
-    if (bh * num_splits > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     const size_t need = attn_decode_workspace_size(B, H, n, m, d_k, d_v);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return ATTN_ERR_INVALID_ARG;
     if (need > 0 && !aligned(workspace, kWsAlign)) return ATTN_ERR_MISALIGNED;
+    if (bh * decode_split_cap(bh, m) > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+    int num_sms = 0;
+    int rc0 = sm_count(&num_sms);
+    if (rc0 != ATTN_OK) return rc0;
+    int split_len = 0, num_splits = 0;
+    decode_split(bh, m, static_cast<int64_t>(num_sms) * (d_k == 64 ? 2 : 1), &split_len, &num_splits);
 
     uint32_t* status = nullptr;
     int rc = status_word(&status);
@@ -666,9 +689,10 @@ extern "C" int attn_decode(const void* Q, const void* K, const void* V, int B, i
     p.O = static_cast<uint16_t*>(O);
     p.LSE = LSE;
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
-    const size_t prow = static_cast<size_t>(bh) * num_splits * n;
-    p.part_o = need > 0 ? reinterpret_cast<float*>(wsb) : nullptr;
-    p.part_ml = need > 0 ? reinterpret_cast<float*>(wsb + round_up(prow * d_k * 4, kWsAlign)) : nullptr;
+    // partials laid out for the cap's chunk count; the launch uses num_splits <= cap of them
+    const size_t prow = static_cast<size_t>(bh) * decode_split_cap(bh, m) * n;
+    p.part_o = num_splits > 1 ? reinterpret_cast<float*>(wsb) : nullptr;
+    p.part_ml = num_splits > 1 ? reinterpret_cast<float*>(wsb + round_up(prow * d_k * 4, kWsAlign)) : nullptr;
     p.status = status;
     p.watchdog_ns = g_watchdog_ns;
     cudaError_t e = attn::launch_decode(d_k, decode_rows(n), tmK, tmV, p, st);
