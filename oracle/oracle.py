@@ -176,3 +176,51 @@ def attn_bwd(Q, K, V, dO, mask="none", key_lengths=None, scale=None, *, threads=
     if rc != 0:
         raise RuntimeError(f"oracle_attn_bwd failed ({rc})")
     return dQ, dK, dV
+
+
+# ------------------------------------------------------------------ projections around the attention
+#
+# "从 RNN 到 Transformer（二）" §4.6 and "Transformer 详解" §4.2: the heads are the
+# projections of the input split per head, W_Q(x).view(B, n, h, d_k).transpose(1, 2),
+# and the output is the heads merged back, out.transpose(1, 2).reshape(B, n, h d_k),
+# followed by W_O. Weights are in the pages' nn.Linear layout [out_features,
+# in_features] (y = x Wᵀ + b); the bias is optional (one page's projections have
+# none, the other's have nn.Linear's default bias). fp64, numpy matmul as the
+# library step.
+
+def _plant_split(y, B, n, H, d, plant):
+    if plant == 12:
+        return y.reshape(B, n, d, H).transpose(0, 3, 1, 2)      # planted: (d, h) order swapped
+    return y.reshape(B, n, H, d).transpose(0, 2, 1, 3)
+
+
+def proj_heads(X, W, bias, H, num_out, *, plant=0):
+    """X [B, n, d_model]; W [num_out*d_model, d_model]; bias [num_out*d_model] or None.
+    Returns num_out arrays [B, H, n, d_model/H]: the projection y = X Wᵀ + b, column
+    block t, split per head."""
+    Xd, Wd = _f64(X), _f64(W)
+    B, n, dm = Xd.shape
+    d = dm // H
+    if plant == 13:
+        y = Xd.reshape(B * n, dm) @ Wd.reshape(dm, -1)          # planted: weight read as [in, out]
+    else:
+        y = Xd.reshape(B * n, dm) @ Wd.T
+    if bias is not None:
+        y = y + _f64(bias)[None, :]
+    outs = []
+    for t in range(num_out):
+        yt = y[:, t * dm:(t + 1) * dm]
+        outs.append(np.ascontiguousarray(_plant_split(yt, B, n, H, d, plant)))
+    return outs
+
+
+def merge_proj(O, W_o, bias, *, plant=0):
+    """O [B, H, n, d]; W_o [d_out, H*d]; bias [d_out] or None. Returns Y [B, n, d_out]:
+    the heads merged back (column h*d + j) times W_oᵀ plus the bias."""
+    Od, Wd = _f64(O), _f64(W_o)
+    B, H, n, d = Od.shape
+    merged = Od.transpose(0, 2, 1, 3).reshape(B * n, H * d)
+    y = merged @ Wd.T
+    if bias is not None:
+        y = y + _f64(bias)[None, :]
+    return y.reshape(B, n, Wd.shape[0])
