@@ -6,11 +6,12 @@ function of the same bf16 inputs. Tolerance, derived from the path's roundings
 (every other error source is below 2^-18 relative): for each gradient G,
 elementwise |G - G_ref| <= 2 * bound + 1e-6 with
 
-  dV: bound = 2^-9 |dV_ref| + 2^-9 (Wᵀ |dO|)        (bf16 output; bf16 P)
-  dK: bound = 2^-9 |dK_ref| + scale * Tᵀ |Q|
-  dQ: bound = 2^-9 |dQ_ref| + scale * T |K|
-      T_ij  = W_ij (2^-9 |dP_ij - D_i| + E_i)        (bf16 dS; D from the bf16 O)
-      E_i   = 2^-8 sum_c |dO_ic| (|O_ic| + A_ic)     (the forward's O error)
+  dV: bound = u |dV_ref| + u (Wᵀ |dO|)              (bf16 output; bf16 P)
+  dK: bound = u |dK_ref| + scale * Tᵀ |Q|
+  dQ: bound = u |dQ_ref| + scale * T |K|
+      T_ij  = W_ij (u |dP_ij - D_i| + E_i)           (bf16 dS; D from the bf16 O)
+      E_i   = u sum_c |dO_ic| (|O_ic| + A_ic)        (the forward's O error)
+      u     = 2^-8, the unit roundoff of bf16 (8-bit significand)
 
 where W are the oracle's weights, dP = dO Vᵀ, D_i = dO_i . O_i, and A = the
 oracle's output on |V| (the sum of w_j |v_j| that bounds the forward's P
@@ -26,7 +27,7 @@ from transformer_scaled_dot_03_gb300 import attn, build, inputs
 
 pytestmark = pytest.mark.gpu
 
-HALF_ULP = 2.0 ** -9
+U = 2.0 ** -8          # unit roundoff of bf16 (8-bit significand)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -54,12 +55,12 @@ def bounds(x: inputs.Inputs, dO: torch.Tensor, refs):
     A, _ = oracle.attn_fwd(x.Q, x.K, x.V.abs(), x.mask, x.key_lengths, x.scale)
     dP = np.einsum("bhic,bhjc->bhij", g, Vd)
     D = np.sum(g * Or, axis=-1)
-    E = 2.0 ** -8 * np.sum(np.abs(g) * (np.abs(Or) + A), axis=-1)
-    T = W * (HALF_ULP * np.abs(dP - D[..., None]) + E[..., None])
+    E = U * np.sum(np.abs(g) * (np.abs(Or) + A), axis=-1)
+    T = W * (U * np.abs(dP - D[..., None]) + E[..., None])
     dQr, dKr, dVr = refs
-    bq = HALF_ULP * np.abs(dQr) + x.scale * np.einsum("bhij,bhjc->bhic", T, np.abs(Kd))
-    bk = HALF_ULP * np.abs(dKr) + x.scale * np.einsum("bhij,bhic->bhjc", T, np.abs(Qd))
-    bv = HALF_ULP * np.abs(dVr) + HALF_ULP * np.einsum("bhij,bhic->bhjc", W, np.abs(g))
+    bq = U * np.abs(dQr) + x.scale * np.einsum("bhij,bhjc->bhic", T, np.abs(Kd))
+    bk = U * np.abs(dKr) + x.scale * np.einsum("bhij,bhic->bhjc", T, np.abs(Qd))
+    bv = U * np.abs(dVr) + U * np.einsum("bhij,bhic->bhjc", W, np.abs(g))
     return bq, bk, bv
 
 
