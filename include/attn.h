@@ -209,6 +209,32 @@ int attn_decode(const void* Q, const void* K, const void* V, int B, int H, int n
                 int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
                 void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * The projections around the attention ("从 RNN 到 Transformer（二）" §4.6,
+ * "Transformer 详解" §4.2): Q = W_Q(x).view(B, n, h, d).transpose(1, 2) (and K, V
+ * likewise) before it, and Y = W_O(out.transpose(1, 2).reshape(B, n, h d)) after
+ * it. Weights are in nn.Linear layout [out_features, in_features] (y = x Wᵀ + b);
+ * the bias is optional (NULL: none). bf16 in and out, fp32 accumulation, one
+ * persistent tensor-core GEMM whose loads and stores do the head split and merge.
+ *
+ * attn_proj_heads: X bf16 [B, n, d_model]; W bf16 [num_out*d_model, d_model]
+ *   (the weights of num_out projections stacked, e.g. W_Q, W_K, W_V); bias bf16
+ *   [num_out*d_model] or NULL; out0..out{num_out-1} bf16 [B, H, n, d_model/H]
+ *   receive column blocks 0..num_out-1 split per head. num_out is 1..3 (3: self-
+ *   attention's Q, K, V; 1 and 2: cross-attention's Q from the decoder and K, V
+ *   from the encoder).
+ * attn_merge_proj: O bf16 [B, H, n, d] (an attention output); W_o bf16
+ *   [d_out, H*d]; bias bf16 [d_out] or NULL; Y bf16 [B, n, d_out].
+ * Supported: d_model/H (resp. d) in {64, 128}; n a multiple of 32; d_out a
+ * multiple of 64 (else ATTN_ERR_UNSUPPORTED). Pointers 16-byte aligned.
+ * Returns ATTN_OK or a negative attn_status_t; on error nothing is enqueued.
+ */
+int attn_proj_heads(const void* X, const void* W, const void* bias, int B, int n, int d_model, int H,
+                    int num_out, void* out0, void* out1, void* out2, void* stream);
+
+int attn_merge_proj(const void* O, const void* W_o, const void* bias, int B, int n, int H, int d,
+                    int d_out, void* Y, void* stream);
+
 /* Human-readable name of a status code. */
 const char* attn_status_string(int status);
 

@@ -175,3 +175,28 @@ def test_decode_workspace_size():
 @pytest.mark.parametrize("kw", [dict(B=0), dict(n=0)])
 def test_decode_empty_is_noop(lib, kw):
     assert call_dec(**kw) == attn.ATTN_OK
+
+
+@pytest.mark.parametrize("args,code", [
+    ((P, P, None, 1, 64, 512, 8, 4, P2, P2, P2), attn.ATTN_ERR_INVALID_ARG),     # num_out 4
+    ((P, P, None, 1, 64, 512, 8, 0, P2, P2, P2), attn.ATTN_ERR_INVALID_ARG),
+    ((P, P, None, 1, 64, 512, 16, 3, P2, P2, P2), attn.ATTN_ERR_UNSUPPORTED),    # head dim 32
+    ((P, P, None, 1, 48, 512, 8, 3, P2, P2, P2), attn.ATTN_ERR_UNSUPPORTED),     # n not a multiple of 32
+    ((P, P, None, 1, 64, 512, 8, 2, P2, None, P2), attn.ATTN_ERR_INVALID_ARG),   # missing output
+    ((P, P, ctypes.c_void_p(0x30008), 1, 64, 512, 8, 1, P2, None, None), attn.ATTN_ERR_MISALIGNED),
+    ((P, P, None, 0, 64, 512, 8, 3, None, None, None), attn.ATTN_OK),             # no rows
+])
+def test_proj_heads_validation(lib, args, code):
+    assert lib.attn_proj_heads(*args, None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((P, P, None, 1, 64, 8, 96, 512, P2), attn.ATTN_ERR_UNSUPPORTED),            # head dim 96
+    ((P, P, None, 1, 64, 8, 64, 100, P2), attn.ATTN_ERR_UNSUPPORTED),            # d_out % 64
+    ((P, P, None, 1, 40, 8, 64, 512, P2), attn.ATTN_ERR_UNSUPPORTED),            # n % 32
+    ((P, P, None, 1, 64, 8, 64, 512, None), attn.ATTN_ERR_INVALID_ARG),
+    ((P, P, None, 1, 64, 8, 64, 512, ctypes.c_void_p(0x20002)), attn.ATTN_ERR_MISALIGNED),
+    ((P, P, None, 1, 0, 8, 64, 512, P2), attn.ATTN_OK),
+])
+def test_merge_proj_validation(lib, args, code):
+    assert lib.attn_merge_proj(*args, None) == code

@@ -34,7 +34,7 @@ MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PAD
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
            "attn_last_error", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
-           "attn_decode_workspace_size")
+           "attn_decode_workspace_size", "attn_proj_heads", "attn_merge_proj")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode.restype = i32
         lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_decode_workspace_size.restype = ctypes.c_size_t
+        lib.attn_proj_heads.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
+        lib.attn_proj_heads.restype = i32
+        lib.attn_merge_proj.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp]
+        lib.attn_merge_proj.restype = i32
         lib.attn_last_error.argtypes = []
         lib.attn_last_error.restype = ctypes.c_char_p
         _lib = lib
@@ -254,6 +258,57 @@ def attn_decode(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode", last_error() if rc == ATTN_ERR_CUDA else "")
     return O, LSE
+
+
+def _bf16_cuda(name, t, dim):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != dim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dim}-D bf16 CUDA tensor")
+
+
+def proj_heads(X: torch.Tensor, W: torch.Tensor, H: int, bias: torch.Tensor | None = None,
+               num_out: int | None = None, outs=None, stream=None):
+    """Input projections with the per-head split: X [B, n, d_model], W [num_out*d_model,
+    d_model] (nn.Linear layout), optional bias [num_out*d_model]; returns num_out tensors
+    [B, H, n, d_model/H] (e.g. Q, K, V). Asynchronous on ``stream``."""
+    _bf16_cuda("X", X, 3)
+    _bf16_cuda("W", W, 2)
+    B, n, d_model = X.shape
+    num_out = W.shape[0] // d_model if num_out is None else num_out
+    if tuple(W.shape) != (num_out * d_model, d_model):
+        raise ValueError("W must be [num_out*d_model, d_model]")
+    if bias is not None:
+        _bf16_cuda("bias", bias, 1)
+        if bias.numel() != num_out * d_model:
+            raise ValueError("bias must be [num_out*d_model]")
+    d = d_model // H if H > 0 else 0
+    if outs is None:
+        outs = [torch.empty((B, H, n, d), dtype=torch.bfloat16, device=X.device) for _ in range(num_out)]
+    ptrs = [_ptr(t) for t in outs] + [None] * (3 - len(outs))
+    rc = load().attn_proj_heads(_ptr(X), _ptr(W), _ptr(bias), int(B), int(n), int(d_model), int(H), int(num_out),
+                                ptrs[0], ptrs[1], ptrs[2], ctypes.c_void_p(_stream_handle(stream)))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_proj_heads", last_error() if rc == ATTN_ERR_CUDA else "")
+    return outs
+
+
+def merge_proj(O: torch.Tensor, W_o: torch.Tensor, bias: torch.Tensor | None = None, Y=None, stream=None):
+    """Output projection of the merged heads: O [B, H, n, d], W_o [d_out, H*d] (nn.Linear
+    layout), optional bias [d_out]; returns Y [B, n, d_out]. Asynchronous on ``stream``."""
+    _bf16_cuda("O", O, 4)
+    _bf16_cuda("W_o", W_o, 2)
+    B, H, n, d = O.shape
+    d_out = W_o.shape[0]
+    if W_o.shape[1] != H * d:
+        raise ValueError("W_o must be [d_out, H*d]")
+    if bias is not None:
+        _bf16_cuda("bias", bias, 1)
+    if Y is None:
+        Y = torch.empty((B, n, d_out), dtype=torch.bfloat16, device=O.device)
+    rc = load().attn_merge_proj(_ptr(O), _ptr(W_o), _ptr(bias), int(B), int(n), int(H), int(d), int(d_out),
+                                _ptr(Y), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_merge_proj", last_error() if rc == ATTN_ERR_CUDA else "")
+    return Y
 
 
 def device_status(stream=None) -> tuple[int, int]:

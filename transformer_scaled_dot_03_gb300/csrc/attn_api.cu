@@ -698,3 +698,133 @@ extern "C" int attn_decode(const void* Q, const void* K, const void* V, int B, i
     cudaError_t e = attn::launch_decode(d_k, decode_rows(n), tmK, tmV, p, st);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("decode kernel launch", e);
 }
+
+// ---------------------------------------------------------------------------
+// Projections around the attention.
+namespace {
+
+// Any-rank tiled map with 128-byte swizzle; dims innermost first, strides in bytes
+// for dims 1..rank-1.
+int encode_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, CUtensorMapDataType type, uint32_t rank,
+               const void* base, const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box)
+{
+    cuuint32_t es[5] = {1u, 1u, 1u, 1u, 1u};
+    CUresult r = enc(map, type, rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (rank %u) failed (%d)", rank,
+                 static_cast<int>(r));
+        return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+}
+
+// [rows][cols] bf16 matrix as a 3-D map {cols, rows, 1} with a {64, box_rows, 1} box.
+int matrix_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* base, int64_t rows,
+               int64_t cols, uint32_t box_rows)
+{
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols * 2), static_cast<cuuint64_t>(rows * cols * 2)};
+    cuuint32_t box[3] = {64u, box_rows, 1u};
+    return encode_map(enc, map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
+}
+
+// [B][H][n][d] bf16 head tensor as a 4-D map with a {64, 32, 1, 1} box.
+int heads_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* base, int64_t B, int64_t H,
+              int64_t n, int64_t d)
+{
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(n * d * 2),
+                             static_cast<cuuint64_t>(H * n * d * 2)};
+    cuuint32_t box[4] = {64u, 32u, 1u, 1u};
+    return encode_map(enc, map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box);
+}
+
+int run_proj(bool heads_in, bool heads_out, attn::ProjMaps& maps, attn::ProjParams& p, cudaStream_t st)
+{
+    uint32_t* status = nullptr;
+    int rc = status_word(&status);
+    if (rc != ATTN_OK) return rc;
+    int num_sms = 0;
+    if ((rc = sm_count(&num_sms)) != ATTN_OK) return rc;
+    p.tiles_m = (p.R + 127) / 128;
+    p.tiles_n = (p.N + 255) / 256;
+    p.status = status;
+    p.watchdog_ns = g_watchdog_ns;
+    cudaError_t e = attn::launch_proj(heads_in, heads_out, maps, p, num_sms, st);
+    return e == cudaSuccess ? ATTN_OK : fail_cuda("projection kernel launch", e);
+}
+
+}  // namespace
+
+extern "C" int attn_proj_heads(const void* X, const void* W, const void* bias, int B, int n, int d_model, int H,
+                               int num_out, void* out0, void* out1, void* out2, void* stream)
+{
+    if (B < 0 || n < 0 || d_model < 1 || H < 1 || num_out < 1 || num_out > 3) return ATTN_ERR_INVALID_ARG;
+    if (d_model % H != 0 || !head_dim_ok(d_model / H)) return ATTN_ERR_UNSUPPORTED;
+    if (n % 32 != 0) return ATTN_ERR_UNSUPPORTED;
+    const int64_t R = static_cast<int64_t>(B) * n;
+    if (R > INT32_MAX / 2 || static_cast<int64_t>(num_out) * d_model > 65536) return ATTN_ERR_UNSUPPORTED;
+    if (R == 0) return ATTN_OK;
+    void* outs[3] = {out0, out1, out2};
+    if (X == nullptr || W == nullptr) return ATTN_ERR_INVALID_ARG;
+    for (int t = 0; t < num_out; ++t)
+        if (outs[t] == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(W, 16) || (bias != nullptr && !aligned(bias, 16))) return ATTN_ERR_MISALIGNED;
+    for (int t = 0; t < num_out; ++t)
+        if (!aligned(outs[t], 16)) return ATTN_ERR_MISALIGNED;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    int rc = encoder(&enc);
+    if (rc != ATTN_OK) return rc;
+    const int d = d_model / H;
+    const int N = num_out * d_model;
+    attn::ProjMaps maps;
+    if ((rc = matrix_map(enc, &maps.a, X, R, d_model, 128)) != ATTN_OK) return rc;
+    if ((rc = matrix_map(enc, &maps.w, W, N, d_model, 256)) != ATTN_OK) return rc;
+    for (int t = 0; t < 3; ++t)
+        if ((rc = heads_map(enc, &maps.c[t], outs[t < num_out ? t : 0], B, H, n, d)) != ATTN_OK) return rc;
+    attn::ProjParams p;
+    p.R = static_cast<int>(R);
+    p.N = N;
+    p.K = d_model;
+    p.n = n;
+    p.H = H;
+    p.d = d;
+    p.d_block = d_model;
+    p.bias = static_cast<const uint16_t*>(bias);
+    return run_proj(false, true, maps, p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int attn_merge_proj(const void* O, const void* W_o, const void* bias, int B, int n, int H, int d,
+                               int d_out, void* Y, void* stream)
+{
+    if (B < 0 || n < 0 || H < 1 || d_out < 1) return ATTN_ERR_INVALID_ARG;
+    if (!head_dim_ok(d) || d_out % 64 != 0 || n % 32 != 0) return ATTN_ERR_UNSUPPORTED;
+    const int64_t R = static_cast<int64_t>(B) * n;
+    if (R > INT32_MAX / 2 || static_cast<int64_t>(H) * d > 65536 || d_out > 65536) return ATTN_ERR_UNSUPPORTED;
+    if (R == 0) return ATTN_OK;
+    if (O == nullptr || W_o == nullptr || Y == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(O, 16) || !aligned(W_o, 16) || !aligned(Y, 16) || (bias != nullptr && !aligned(bias, 16)))
+        return ATTN_ERR_MISALIGNED;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    int rc = encoder(&enc);
+    if (rc != ATTN_OK) return rc;
+    const int K = H * d;
+    attn::ProjMaps maps;
+    if ((rc = heads_map(enc, &maps.a, O, B, H, n, d)) != ATTN_OK) return rc;
+    if ((rc = matrix_map(enc, &maps.w, W_o, d_out, K, 256)) != ATTN_OK) return rc;
+    if ((rc = matrix_map(enc, &maps.c[0], Y, R, d_out, 32)) != ATTN_OK) return rc;
+    maps.c[1] = maps.c[0];
+    maps.c[2] = maps.c[0];
+    attn::ProjParams p;
+    p.R = static_cast<int>(R);
+    p.N = d_out;
+    p.K = K;
+    p.n = n;
+    p.H = H;
+    p.d = d;
+    p.d_block = d_out;
+    p.bias = static_cast<const uint16_t*>(bias);
+    return run_proj(true, false, maps, p, static_cast<cudaStream_t>(stream));
+}

@@ -102,6 +102,25 @@ struct DecodeParams {
 cudaError_t launch_decode(int d, int rows, const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p,
                           cudaStream_t stream);
 
+// Projections around the attention (attn_kernel_proj.cuh): Y = A Wᵀ (+ bias).
+struct ProjParams {
+    int R, N, K;                  // rows (B*n), output columns, reduction length
+    int n, H, d;                  // rows per batch entry, heads, head dim (head-shaped operands)
+    int d_block;                  // output columns per head-split output (d_model)
+    int tiles_m, tiles_n;
+    const uint16_t* bias;         // bf16 [N] or null
+    uint32_t* status;
+    uint64_t watchdog_ns;
+};
+
+struct ProjMaps {
+    CUtensorMap a, w, c[3];
+};
+
+// heads_in: A is O [B,H,n,d] read merged; heads_out: Y split per head into c[0..2].
+cudaError_t launch_proj(bool heads_in, bool heads_out, const ProjMaps& maps, const ProjParams& p, int num_sms,
+                        cudaStream_t stream);
+
 // num_ctas: grid of the one-unit-per-CTA variants; num_sms sizes the persistent grid.
 // The NT variants take d_k = d_v, masks none / causal (n = m) / key padding.
 cudaError_t launch_fwd_d64(int mask, int variant, const TensorMaps& maps, const FwdParams& p,

@@ -183,6 +183,19 @@ def make_grad_output(B, H, n, d_v, seed, value_scale=1.0) -> torch.Tensor:
     return _normal(g, (B, H, n, d_v), value_scale)
 
 
+def make_linear(out_features, in_features, seed, bias=False):
+    """bf16 nn.Linear-layout weight [out, in], Xavier-uniform (bound sqrt(6/(in+out))), and
+    if asked a bias [out] drawn U(-1/sqrt(in), 1/sqrt(in)) (nn.Linear's default bias range)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    bound = math.sqrt(6.0 / (in_features + out_features))
+    W = ((torch.rand(out_features, in_features, generator=g, dtype=torch.float32) * 2.0 - 1.0) * bound)
+    b = None
+    if bias:
+        bb = 1.0 / math.sqrt(in_features)
+        b = ((torch.rand(out_features, generator=g, dtype=torch.float32) * 2.0 - 1.0) * bb).to(torch.bfloat16)
+    return W.to(torch.bfloat16), b
+
+
 def make_projection_inputs(B, H, n, d_model, mask, seed, len_lo, len_hi) -> Inputs:
     """Base-encoder recipe: X ~ N(0,1) [B,n,d_model]; W_Q, W_K, W_V Xavier-uniform
     [d_model, d_model] with bound sqrt(6/(2*d_model)), no bias ("Transformer 详解"
