@@ -41,6 +41,8 @@ from transformer_scaled_dot_03_gb300 import inputs  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (bf16) at 1 GB300 and % of dense BF16 tensor peak"
 METRIC_BWD = "attention bwd TFLOP/s (bf16; nominal 2.5x the forward's FLOPs) at 1 GB300"
+METRIC_PROJ = {"proj": "QKV projection + head split TFLOP/s (bf16) at 1 GB300",
+               "outproj": "head merge + output projection TFLOP/s (bf16) at 1 GB300"}
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "base_encoder_keypad"
 L2_BYTES = 129 * 1024 * 1024
@@ -179,13 +181,27 @@ def run_ours(args):
 
     w, x = make_workload(args.workload)
     bwd = args.pass_ == "bwd"
-    decode = w.path == "decode" and not bwd
-    # the backward's five products against the forward's two: 2.5x the nominal FLOPs
-    flops = w.flops() * (2.5 if bwd else 1.0)
-    eff_flops = effective_flops(w, x) * (2.5 if bwd else 1.0)
+    proj = args.pass_ in ("proj", "outproj")
+    decode = w.path == "decode" and not bwd and not proj
+    d_model = w.H * w.d_k
+    if proj and (w.n != w.m or w.d_k != w.d_v or w.n % 32 != 0):
+        raise SystemExit(f"--pass {args.pass_} needs a self-attention workload with n % 32 == 0")
+    if args.pass_ == "proj":
+        # X [B, n, d_model] times the stacked W_Q, W_K, W_V [3 d_model, d_model]
+        flops = eff_flops = 2.0 * w.B * w.n * 3 * d_model * d_model
+    elif args.pass_ == "outproj":
+        flops = eff_flops = 2.0 * w.B * w.n * d_model * d_model
+    else:
+        # the backward's five products against the forward's two: 2.5x the nominal FLOPs
+        flops = w.flops() * (2.5 if bwd else 1.0)
+        eff_flops = effective_flops(w, x) * (2.5 if bwd else 1.0)
     qkv_bytes = x.Q.numel() * 2 + x.K.numel() * 2 + x.V.numel() * 2
     o_bytes = w.B * w.H * w.n * (w.d_v * 2 + 4)
-    if bwd:
+    if args.pass_ == "proj":
+        in_bytes, out_bytes = w.B * w.n * d_model * 2, qkv_bytes
+    elif args.pass_ == "outproj":
+        in_bytes = out_bytes = w.B * w.n * d_model * 2
+    elif bwd:
         # inputs Q, K, V, O, LSE, dO; outputs dQ, dK, dV
         in_bytes = qkv_bytes + o_bytes + w.B * w.H * w.n * w.d_v * 2
         out_bytes = qkv_bytes
@@ -196,8 +212,20 @@ def run_ours(args):
     lens_d = x.key_lengths.to(dev) if x.key_lengths is not None else None
     dO_h = inputs.make_grad_output(w.B, w.H, w.n, w.d_v, seed=100 + w.seed) if bwd else None
     sets = []
+    if proj:
+        Wp, bp = inputs.make_linear((3 if args.pass_ == "proj" else 1) * d_model, d_model, seed=200 + w.seed,
+                                    bias=True)
+        Wp, bp = Wp.to(dev), bp.to(dev)
+        a_h = inputs.make_inputs(w.B, 1, w.n, 1, d_model, d_model, seed=300 + w.seed).Q[:, 0].contiguous() \
+            if args.pass_ == "proj" else x.Q
     with torch.cuda.stream(stream):
-        for _ in range(copies):
+        for _ in range(copies if proj else 0):
+            if args.pass_ == "proj":
+                sets.append((a_h.to(dev), torch.empty_like(x.Q, device=dev), torch.empty_like(x.K, device=dev),
+                             torch.empty_like(x.V, device=dev)))
+            else:
+                sets.append((a_h.to(dev), torch.empty(w.B, w.n, d_model, dtype=torch.bfloat16, device=dev)))
+        for _ in range(0 if proj else copies):
             st = [x.Q.to(dev), x.K.to(dev), x.V.to(dev),
                   torch.empty(w.B, w.H, w.n, w.d_v, dtype=torch.bfloat16, device=dev),
                   torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)]
@@ -205,7 +233,9 @@ def run_ours(args):
                 attn.attn_fwd(st[0], st[1], st[2], w.mask, lens_d, x.scale, O=st[3], LSE=st[4], stream=stream)
                 st += [dO_h.to(dev), torch.empty_like(st[0]), torch.empty_like(st[1]), torch.empty_like(st[2])]
             sets.append(tuple(st))
-    if bwd:
+    if proj:
+        ws_bytes, launches_per_step = 0, 1
+    elif bwd:
         ws_bytes = attn.bwd_workspace_size(w.B, w.H, w.n, w.m, w.d_k, w.d_v)
         launches_per_step = 3                        # preparation, main kernel, dQ conversion
     elif decode:
@@ -217,7 +247,13 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
 
     def run(st, lens):
-        if bwd:
+        if args.pass_ == "proj":
+            X, Q, K, V = st
+            attn.proj_heads(X, Wp, w.H, bp, 3, outs=[Q, K, V], stream=stream)
+        elif args.pass_ == "outproj":
+            O, Y = st
+            attn.merge_proj(O, Wp, bp, Y=Y, stream=stream)
+        elif bwd:
             Q, K, V, O, L, dO, dQ, dK, dV = st
             attn.attn_bwd(Q, K, V, O, L, dO, w.mask, lens, x.scale, dQ, dK, dV, workspace=ws, stream=stream)
         elif decode:
@@ -275,7 +311,7 @@ def run_ours(args):
     # end to end through the C entry point with pinned host buffers: every input of
     # the pass host -> device, the pass, every output device -> host
     dev_set = sets[0]
-    n_in = 6 if bwd else 3                   # Q, K, V (+ O, LSE, dO for the backward)
+    n_in = 1 if proj else (6 if bwd else 3)  # X or O; Q, K, V (+ O, LSE, dO for the backward)
     host_in = [t.cpu().pin_memory() for t in dev_set[:n_in]]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_set[n_in:]]
     hlens = x.key_lengths.pin_memory() if x.key_lengths is not None else None
@@ -321,7 +357,7 @@ def run_ours(args):
 
     # the committed traffic figure belongs to the forward tensor-core kernel
     traffic = args.traffic if args.traffic is not None else (
-        None if (bwd or decode) else measured_traffic(w.name))
+        None if (bwd or decode or proj) else measured_traffic(w.name))
     if decode:
         roofline = {"bound": "hbm", "achieved": round(hbm_gbs, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(hbm_gbs / hbm, 4), "traffic": traffic,
@@ -339,15 +375,16 @@ def run_ours(args):
     result = None
     if rank == 0:
         cpu = None
-        if world == 1 and not args.no_cpu_baseline and not bwd:
+        if world == 1 and not args.no_cpu_baseline and not bwd and not proj:
             cpu = cpu_baseline(w, x, args.cpu_seconds)
         clocks = clk.summary()
         result = {
-            "metric": METRIC_BWD if bwd else METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC_BWD if bwd else (METRIC_PROJ[args.pass_] if proj else METRIC),
+            "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; bias-free Xavier projections of X~N(0,1))",
-            "config": {"workload": w.name, "pass": "bwd" if bwd else ("decode" if decode else "fwd"),
+            "config": {"workload": w.name, "pass": args.pass_ if (bwd or proj) else ("decode" if decode else "fwd"),
                        "B": w.B, "H": w.H, "n": w.n, "m": w.m,
                        "d_k": w.d_k, "d_v": w.d_v, "mask": w.mask,
                        "key_lengths": [w.len_lo, w.len_hi] if w.mask in inputs.LENGTH_MASKS else None,
@@ -463,8 +500,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER + inputs.VARIANT_ORDER + inputs.DECODE_ORDER)
     ap.add_argument("--e2e-steps", type=int, default=50)
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
-                    help="fwd: the forward (the headline); bwd: the backward of the same workload")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "proj", "outproj"], default="fwd",
+                    help="fwd: the forward (the headline); bwd: the backward of the same workload; "
+                         "proj / outproj: the projections around it (weights resident)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,

@@ -729,15 +729,15 @@ int matrix_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const vo
     return encode_map(enc, map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
 }
 
-// [B][H][n][d] bf16 head tensor as a 4-D map with a {64, 32, 1, 1} box.
+// [B][H][n][d] bf16 head tensor as a 4-D map with a {64, box_rows, 1, 1} box.
 int heads_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, const void* base, int64_t B, int64_t H,
-              int64_t n, int64_t d)
+              int64_t n, int64_t d, uint32_t box_rows)
 {
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(B)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(d * 2), static_cast<cuuint64_t>(n * d * 2),
                              static_cast<cuuint64_t>(H * n * d * 2)};
-    cuuint32_t box[4] = {64u, 32u, 1u, 1u};
+    cuuint32_t box[4] = {64u, box_rows, 1u, 1u};
     return encode_map(enc, map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box);
 }
 
@@ -783,7 +783,7 @@ extern "C" int attn_proj_heads(const void* X, const void* W, const void* bias, i
     if ((rc = matrix_map(enc, &maps.a, X, R, d_model, 128)) != ATTN_OK) return rc;
     if ((rc = matrix_map(enc, &maps.w, W, N, d_model, 256)) != ATTN_OK) return rc;
     for (int t = 0; t < 3; ++t)
-        if ((rc = heads_map(enc, &maps.c[t], outs[t < num_out ? t : 0], B, H, n, d)) != ATTN_OK) return rc;
+        if ((rc = heads_map(enc, &maps.c[t], outs[t < num_out ? t : 0], B, H, n, d, 32)) != ATTN_OK) return rc;
     attn::ProjParams p;
     p.R = static_cast<int>(R);
     p.N = N;
@@ -792,6 +792,7 @@ extern "C" int attn_proj_heads(const void* X, const void* W, const void* bias, i
     p.H = H;
     p.d = d;
     p.d_block = d_model;
+    p.a_box_rows = 128;
     p.bias = static_cast<const uint16_t*>(bias);
     return run_proj(false, true, maps, p, static_cast<cudaStream_t>(stream));
 }
@@ -812,7 +813,8 @@ extern "C" int attn_merge_proj(const void* O, const void* W_o, const void* bias,
     if (rc != ATTN_OK) return rc;
     const int K = H * d;
     attn::ProjMaps maps;
-    if ((rc = heads_map(enc, &maps.a, O, B, H, n, d)) != ATTN_OK) return rc;
+    const uint32_t a_rows = n % 128 == 0 ? 128u : 32u;
+    if ((rc = heads_map(enc, &maps.a, O, B, H, n, d, a_rows)) != ATTN_OK) return rc;
     if ((rc = matrix_map(enc, &maps.w, W_o, d_out, K, 256)) != ATTN_OK) return rc;
     if ((rc = matrix_map(enc, &maps.c[0], Y, R, d_out, 32)) != ATTN_OK) return rc;
     maps.c[1] = maps.c[0];
@@ -825,6 +827,7 @@ extern "C" int attn_merge_proj(const void* O, const void* W_o, const void* bias,
     p.H = H;
     p.d = d;
     p.d_block = d_out;
+    p.a_box_rows = static_cast<int>(a_rows);
     p.bias = static_cast<const uint16_t*>(bias);
     return run_proj(true, false, maps, p, static_cast<cudaStream_t>(stream));
 }

@@ -107,6 +107,7 @@ struct ProjParams {
     int R, N, K;                  // rows (B*n), output columns, reduction length
     int n, H, d;                  // rows per batch entry, heads, head dim (head-shaped operands)
     int d_block;                  // output columns per head-split output (d_model)
+    int a_box_rows;               // head-shaped A: rows per 4-D load box (128 when n % 128 == 0, else 32)
     int tiles_m, tiles_n;
     const uint16_t* bias;         // bf16 [N] or null
     uint32_t* status;

@@ -10,8 +10,10 @@
 //
 //   A_HEADS = false  A is a plain [R, K] matrix (the input x)
 //   A_HEADS = true   A is the attention output O [B, H, n, d] read as [R, H·d]:
-//                    each 64-column chunk of A is one head's slice, loaded as four
-//                    32-row boxes of a 4-D tensor map (the merge costs nothing)
+//                    each 64-column chunk of A is one head's slice, loaded as one
+//                    128-row box of a 4-D tensor map when n is a multiple of 128
+//                    (a row tile then lies in one batch entry), else as four
+//                    32-row boxes (the merge costs nothing)
 //   C_HEADS = false  Y is a plain [R, N] matrix
 //   C_HEADS = true   Y's column block t (of width d_model) is written to output t
 //                    in [B, H, n, d] (the split costs nothing: every 64-column,
@@ -114,8 +116,9 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int m0 = (tile / p.tiles_n) * BM;
                 const int n0 = (tile % p.tiles_n) * BN;
-                // A_HEADS: 32-row groups that hold rows (the rest of the smem tile is never stored)
-                const int groups = A_HEADS ? min(4, (p.R - m0 + 31) / 32) : 4;
+                // A_HEADS in 32-row boxes: the groups that hold rows (the rest of the smem
+                // tile is never stored)
+                const int groups = (A_HEADS && p.a_box_rows == 32) ? min(4, (p.R - m0 + 31) / 32) : 4;
                 for (int kc = 0; kc < nk; ++kc, ++it) {
                     const int s = it % STAGES;
                     if (it >= STAGES &&
@@ -125,13 +128,18 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
                         break;
                     }
                     const uint32_t sa = sbase + A_OFF + s * A_BYTES;
-                    mbar_arrive_expect_tx(bar(B_FULL + s), (A_HEADS ? groups * ST_BYTES : A_BYTES) + B_BYTES);
+                    mbar_arrive_expect_tx(bar(B_FULL + s), groups * ST_BYTES + B_BYTES);
                     if (A_HEADS) {
                         const int c = kc * BK;
                         const int h = c / p.d, j0 = c % p.d;
-                        for (int g = 0; g < groups; ++g) {
-                            const int r0 = m0 + 32 * g;
-                            tma_load_4d(sa + g * ST_BYTES, &maps.a, bar(B_FULL + s), j0, r0 % p.n, h, r0 / p.n);
+                        if (p.a_box_rows == 128) {
+                            tma_load_4d(sa, &maps.a, bar(B_FULL + s), j0, m0 % p.n, h, m0 / p.n);
+                        } else {
+                            for (int g = 0; g < groups; ++g) {
+                                const int r0 = m0 + 32 * g;
+                                tma_load_4d(sa + g * ST_BYTES, &maps.a, bar(B_FULL + s), j0, r0 % p.n, h,
+                                            r0 / p.n);
+                            }
                         }
                     } else {
                         tma_load_3d(sa, &maps.a, bar(B_FULL + s), kc * BK, m0, 0);
