@@ -21,16 +21,20 @@
 // accumulator in global memory (every key tile of the head adds to it). D and
 // LSE·log2(e) come from a preparation kernel, padded to whole query tiles.
 //
-//   warps 0-3   Pᵀ/dSᵀ (thread = key), dQ read-out (thread = query), dK/dV epilogue
-//   warp  4     TMA producer: K and V once, then Q, dO, LSE, D per query tile
-//   warp  5     tcgen05.mma issuer, owns the TMEM allocation
-//   warps 6-7   idle
+//   warps 0-7   Pᵀ/dSᵀ (thread = key), dQ read-out (thread = query), dK/dV epilogue;
+//               warp w serves tensor-memory lanes 32(w % 4)..+31 and the half
+//               w / 4 of the columns (queries for Pᵀ/dSᵀ, head dims for dQ, dK, dV):
+//               every element of Pᵀ and dSᵀ is independent (P comes from the saved
+//               LSE), so two warpgroups share a row without exchanging anything
+//   warp  8     TMA producer: K and V once, then Q, dO, LSE, D per query tile
+//   warp  9     tcgen05.mma issuer, owns the TMEM allocation
 // Tensor memory (512 columns): Sᵀ [0,128) then Pᵀ [0,64); dPᵀ [128,256) then dSᵀ
 // [128,192); dV [256,256+d); dK [256+d,256+2d); dQ at d = 64 in [384,448), at
 // d = 128 as two 64-column halves in [64,128) and [192,256).
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -51,9 +55,10 @@ template <int D>
 struct Layout {
     static constexpr int CH = D / 64;
     static constexpr int TILE = CH * CHUNK_BYTES;        // a 128 x D bf16 tile
-    static constexpr int NUM_THREADS = 256;
-    static constexpr int WARP_TMA = 4;
-    static constexpr int WARP_MMA = 5;
+    static constexpr int NUM_THREADS = 320;
+    static constexpr int COMPUTE_THREADS = 256;
+    static constexpr int WARP_TMA = 8;
+    static constexpr int WARP_MMA = 9;
     static constexpr int QS = D == 64 ? 2 : 1;             // Q/dO/LSE/D ring depth
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + TILE;
@@ -72,7 +77,9 @@ struct Layout {
     static constexpr int B_DQFREE = B_DQFULL + 1;   // dQ read out of TMEM        (128 arrivals)
     static constexpr int B_TILEDONE = B_DQFREE + 1; // every MMA of the tile done (commit)
     static constexpr int B_DKVDONE = B_TILEDONE + 1;
-    static constexpr int B_NEVER = B_DKVDONE + 1;
+    static constexpr int B_RDONE = B_DKVDONE + 1;   // Sᵀ and dPᵀ of the tile read    (256 arrivals)
+    static constexpr int B_EPI = B_RDONE + 1;       // epilogue staging steps         (256 arrivals)
+    static constexpr int B_NEVER = B_EPI + 1;
     static constexpr int NBARS = B_NEVER + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16 + 1024;
@@ -147,11 +154,13 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             mbar_init(bar(L::B_QEMPTY + s), 1);
         }
         mbar_init(bar(L::B_SFULL), 1);
-        mbar_init(bar(L::B_PFULL), BN);
+        mbar_init(bar(L::B_PFULL), L::COMPUTE_THREADS);
         mbar_init(bar(L::B_DQFULL), 1);
-        mbar_init(bar(L::B_DQFREE), BN);
+        mbar_init(bar(L::B_DQFREE), L::COMPUTE_THREADS);
         mbar_init(bar(L::B_TILEDONE), 1);
         mbar_init(bar(L::B_DKVDONE), 1);
+        mbar_init(bar(L::B_RDONE), L::COMPUTE_THREADS);
+        mbar_init(bar(L::B_EPI), L::COMPUTE_THREADS);
         mbar_init(bar(L::B_NEVER), 1);
         *abort_word = 0u;
         fence_mbar_init();
@@ -180,7 +189,7 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     const uint32_t sdO = sbase + L::DO_OFF;
     const uint32_t sdS = sbase + L::DS_OFF;
 
-    if (warp >= 4) {
+    if (warp >= L::WARP_TMA) {
         if (warp == L::WARP_TMA && lane == 0) {
             // ================================================== TMA producer
             mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
@@ -283,12 +292,23 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         __syncwarp();
     } else {
         // ================================================== Pᵀ / dSᵀ, dQ read-out, epilogue
-        const int r = 32 * warp + lane;               // TMEM lane: a key here, a query row for dQ
+        const int wq = warp % 4;                      // lane quadrant
+        const int half = warp / 4;                    // column half
+        const int r = 32 * wq + lane;                 // TMEM lane: a key here, a query row for dQ
         const int key = k0 + r;
-        const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
         const float sl2 = p.scale_log2;
         bool ok = true;
         bool store_pending = false;
+        // Rendezvous of the eight compute warps through an mbarrier (every thread
+        // arrives, then waits with the usual bound), so that a warp leaving on a
+        // timeout cannot strand the others.
+        auto rendezvous = [&](int b, uint32_t parity) -> bool {
+            mbar_arrive(bar(b));
+            const bool r = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
+            return __all_sync(0xffffffffu, r);
+        };
+        int epi_phase = 0;
 
         if (p.debug_flags & DEBUG_FORCE_TIMEOUT) {
             ok = mbar_wait(bar(L::B_NEVER), 0, abort_word, p.status, STATUS_FORCED, 20000000ull);
@@ -309,20 +329,22 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            wait_stores_read();   // this warp's staging rows (the dS rows it writes) are free again
-            const uint32_t lse_s = sbase + L::LSE_OFF + s * BM * 4;
-            const uint32_t dd_s = sbase + L::DD_OFF + s * BM * 4;
-            const bool need_mask = __any_sync(0xffffffffu, key >= kv_len || q0 + BM - 1 >= p.n ||
-                                                               (mask_is_causal(MASK) && key > q0 + p.causal_off));
-            // Pᵀ: the whole row of Sᵀ (this key against the tile's 128 queries) at once
-            uint32_t sr[BM];
-            tmem_ld32(tmem + lane_base + L::S_COL + 0, sr + 0);
-            tmem_ld32(tmem + lane_base + L::S_COL + 32, sr + 32);
-            tmem_ld32(tmem + lane_base + L::S_COL + 64, sr + 64);
-            tmem_ld32(tmem + lane_base + L::S_COL + 96, sr + 96);
+            const int c0 = 64 * half;                 // this warpgroup's first query column
+            const uint32_t lse_s = sbase + L::LSE_OFF + (s * BM + c0) * 4;
+            const uint32_t dd_s = sbase + L::DD_OFF + (s * BM + c0) * 4;
+            const bool need_mask =
+                __any_sync(0xffffffffu, key >= kv_len || q0 + c0 + 63 >= p.n ||
+                                            (mask_is_causal(MASK) && key > q0 + c0 + p.causal_off));
+            // this warpgroup's half of the row of Sᵀ and of dPᵀ (64 queries each)
+            uint32_t sr[64], dr[64];
+            tmem_ld32(tmem + lane_base + L::S_COL + c0, sr);
+            tmem_ld32(tmem + lane_base + L::S_COL + c0 + 32, sr + 32);
+            tmem_ld32(tmem + lane_base + L::DP_COL + c0, dr);
+            tmem_ld32(tmem + lane_base + L::DP_COL + c0 + 32, dr + 32);
             tmem_wait_ld();
+            // P = exp2(S·scale·log2 e − LSE·log2 e)
 #pragma unroll
-            for (int c = 0; c < BM / 32; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 float lz[32];
 #pragma unroll
                 for (int v = 0; v < 8; ++v) lds_v4f(lse_s + (32 * c + 4 * v) * 4, lz + 4 * v);
@@ -333,48 +355,50 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 }
             }
             if (need_mask) {
-                // this key is visible to the tile's query columns j in [j_lo, j_hi)
+                // this key is visible to the query columns j in [j_lo, j_hi) of the tile
                 const int q_first = key >= kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - p.causal_off : 0);
-                const int j_lo = q_first == INT32_MAX ? BM : max(q_first - q0, 0);
-                const int j_hi = min(p.n - q0, BM);
+                const int j_lo = q_first == INT32_MAX ? BM : max(q_first - q0, 0) - c0;
+                const int j_hi = min(p.n - q0, BM) - c0;
 #pragma unroll
-                for (int j = 0; j < BM; ++j)
+                for (int j = 0; j < 64; ++j)
                     if (j < j_lo || j >= j_hi) sr[j] = 0u;
             }
+            // dS = P ∘ (dP − D), kept in dr
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int c = 0; c < 2; ++c) {
+                float dz[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) lds_v4f(dd_s + (32 * c + 4 * v) * 4, dz + 4 * v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = 32 * c + i;
+                    dr[j] = __float_as_uint(__uint_as_float(sr[j]) * (__uint_as_float(dr[j]) - dz[i]));
+                }
+            }
+            // Pᵀ and dSᵀ go over the first columns of Sᵀ and dPᵀ, which the other
+            // warpgroup reads: every read of this tile's Sᵀ and dPᵀ comes first
+            ok = rendezvous(L::B_RDONE, parity);
+            if (!ok) break;
+            {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(sr[64 * h + 2 * i]), __uint_as_float(sr[64 * h + 2 * i + 1]));
-                tmem_st32(tmem + lane_base + L::P_COL + 32 * h, pk);   // over Sᵀ, already read
-            }
-            // dSᵀ = Pᵀ ∘ (dPᵀ - D), 32 queries at a time; dSᵀ goes over the dPᵀ columns
-            // already read and, MN-major (row = key, 64-query chunks), into shared memory
+                    pk[i] = pack_bf16x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+                tmem_st32(tmem + lane_base + L::P_COL + 32 * half, pk);
 #pragma unroll
-            for (int c = 0; c < BM / 32; ++c) {
-                uint32_t dr[32];
-                float dz[32];
-                tmem_ld32(tmem + lane_base + L::DP_COL + 32 * c, dr);
+                for (int i = 0; i < 32; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
+                tmem_st32(tmem + lane_base + L::DS_COL + 32 * half, pk);
+                // this warp's staging rows (the dS rows it writes) must have been read by
+                // the previous tile's dQ reduce-add
+                wait_stores_read();
+                // dS, MN-major: row = key r, chunk = this warpgroup's 64 queries
+                const uint32_t row_base = sdS + half * CHUNK_BYTES + r * 128;
 #pragma unroll
-                for (int v = 0; v < 8; ++v) lds_v4f(dd_s + (32 * c + 4 * v) * 4, dz + 4 * v);
-                tmem_wait_ld();
-                uint32_t dk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float a = __uint_as_float(sr[32 * c + 2 * i]) * (__uint_as_float(dr[2 * i]) - dz[2 * i]);
-                    const float b =
-                        __uint_as_float(sr[32 * c + 2 * i + 1]) * (__uint_as_float(dr[2 * i + 1]) - dz[2 * i + 1]);
-                    dk[i] = pack_bf16x2(a, b);
-                }
-                tmem_st16(tmem + lane_base + L::DS_COL + 16 * c, dk);
-                const uint32_t row_base = sdS + (c / 2) * CHUNK_BYTES + r * 128;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t piece = static_cast<uint32_t>((c % 2) * 4 + q);
-                    const uint32_t addr = row_base + ((piece ^ static_cast<uint32_t>(r & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(dk[4 * q]),
-                                 "r"(dk[4 * q + 1]), "r"(dk[4 * q + 2]), "r"(dk[4 * q + 3])
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t addr = row_base + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * q]),
+                                 "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
                                  : "memory");
                 }
             }
@@ -388,35 +412,31 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            // d = 64: this warpgroup's 32 of the 64 dQ columns; d = 128: its 64 (two chunks
+            // of 32, one after the other through this warp's staging rows)
 #pragma unroll 1
-            for (int h = 0; h < D / 64; ++h) {
-                uint32_t a[32], b[32];
-                tmem_ld32(tmem + lane_base + L::dq_col(h), a);
-                tmem_ld32(tmem + lane_base + L::dq_col(h) + 32, b);
+            for (int k = 0; k < D / 64; ++k) {
+                const int col = D == 64 ? 32 * half : 64 * half + 32 * k;   // dQ column of the chunk
+                uint32_t a[32];
+                tmem_ld32(tmem + lane_base + L::dq_col(col / 64) + (col % 64), a);
                 tmem_wait_ld();
-                if (h == D / 64 - 1) {
+                if (k == D / 64 - 1) {
                     tc_fence_before();
                     mbar_arrive(bar(L::B_DQFREE));
                 }
                 wait_stores_read();
+                const uint32_t row_base = sdS + half * CHUNK_BYTES + r * 128;
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const uint32_t* src = cc == 0 ? a : b;
-                    const uint32_t row_base = sdS + cc * CHUNK_BYTES + r * 128;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint32_t addr = row_base + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(src[4 * q]),
-                                     "r"(src[4 * q + 1]), "r"(src[4 * q + 2]), "r"(src[4 * q + 3])
-                                     : "memory");
-                    }
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t addr = row_base + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a[4 * q]),
+                                 "r"(a[4 * q + 1]), "r"(a[4 * q + 2]), "r"(a[4 * q + 3])
+                                 : "memory");
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && q0 + 32 * warp < p.n) {
-                    for (int cc = 0; cc < 2; ++cc)
-                        tma_reduce_add_3d(&maps.dq_acc, sdS + cc * CHUNK_BYTES + warp * 32 * 128, 64 * h + 32 * cc,
-                                          q0 + 32 * warp, bh);
+                if (lane == 0 && q0 + 32 * wq < p.n) {
+                    tma_reduce_add_3d(&maps.dq_acc, sdS + half * CHUNK_BYTES + wq * 32 * 128, col, q0 + 32 * wq, bh);
                     bulk_commit_group();
                     store_pending = true;
                 }
@@ -425,6 +445,8 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         }
 
         // ---------------------------------------- dV, then dK (x scale): TMEM -> bf16 staging -> TMA store
+        // Each warpgroup converts its half of the columns; at d = 64 the two halves
+        // share one 64-column staging chunk and warpgroup 0 stores it.
         if (ok) {
             ok = mbar_wait(bar(L::B_DKVDONE), 0, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
             ok = __all_sync(0xffffffffu, ok);
@@ -436,12 +458,16 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 const uint32_t col = which == 0 ? L::DV_COL : L::DK_COL;
                 const float mul = which == 0 ? 1.f : p.scale;
                 wait_stores_read();
+                // both warpgroups' earlier stores have read the staging
+                ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
+                if (!ok) break;
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    const int c = half * (D / 2) + 32 * cc;   // first column of this 32-column piece
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_base + col + 32 * cc, o);
+                    tmem_ld32(tmem + lane_base + col + c, o);
                     tmem_wait_ld();
-                    const uint32_t chunk_base = sdS + (cc / 2) * CHUNK_BYTES + r * 128;
+                    const uint32_t chunk_base = sdS + (c / 64) * CHUNK_BYTES + r * 128;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint32_t v[4];
@@ -449,7 +475,7 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                         for (int e = 0; e < 4; ++e)
                             v[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * mul,
                                                __uint_as_float(o[8 * q + 2 * e + 1]) * mul);
-                        const uint32_t piece = static_cast<uint32_t>((cc % 2) * 4 + q);
+                        const uint32_t piece = static_cast<uint32_t>(((c % 64) / 32) * 4 + q);
                         const uint32_t addr = chunk_base + ((piece ^ static_cast<uint32_t>(r & 7)) << 4);
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
                                      "r"(v[2]), "r"(v[3])
@@ -457,13 +483,465 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     }
                 }
                 fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && k0 + 32 * warp < p.m) {
+                // both halves of every staged row are written
+                ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
+                if (!ok) break;
+                const bool storer = D == 64 ? half == 0 : true;
+                if (storer && lane == 0 && k0 + 32 * wq < p.m) {
                     const CUtensorMap* map = which == 0 ? &maps.dv : &maps.dk;
-                    for (int c = 0; c < L::CH; ++c)
-                        tma_store_3d(map, sdS + c * CHUNK_BYTES + warp * 32 * 128, c * 64, k0 + 32 * warp, bh);
+                    const int c = D == 64 ? 0 : half;
+                    tma_store_3d(map, sdS + c * CHUNK_BYTES + wq * 32 * 128, c * 64, k0 + 32 * wq, bh);
                     bulk_commit_group();
                     store_pending = true;
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) bulk_wait_group0();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == L::WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// d = 64: the same computation with the query tiles pipelined. dK += dSᵀ Q takes
+// dS from shared memory (the tile written for dQ, row = key with the queries
+// contiguous, is exactly the K-major layout of A = dSᵀ), so dSᵀ needs no tensor
+// memory and Pᵀ gets columns of its own. Then nothing the MMAs of tile t read
+// overlaps what Sᵀ and dPᵀ of tile t+1 write, and the MMA warp issues
+//     Sᵀ, dPᵀ (t+1)   as soon as the softmax warps have loaded Sᵀ, dPᵀ (t)
+//     dV, dK, dQ (t)  once Pᵀ (t) and dS (t) are written,
+// so the tensor cores compute tile t+1's scores while the softmax warps turn tile
+// t's into Pᵀ and dS. The dQ of tile t is read out one iteration later (after
+// tile t+1's Pᵀ and dS), through a staging area of its own.
+//   Tensor memory: Sᵀ [0,128), dPᵀ [128,256), dV [256,320), dK [320,384),
+//   dQ [384,448), Pᵀ [448,512).
+struct LayoutPipe {
+    static constexpr int D = 64;
+    static constexpr int TILE = CHUNK_BYTES;                 // a 128 x 64 bf16 tile
+    static constexpr int NUM_THREADS = 320;
+    static constexpr int COMPUTE_THREADS = 256;
+    static constexpr int WARP_TMA = 8;
+    static constexpr int WARP_MMA = 9;
+    static constexpr int QS = 2;
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = K_OFF + TILE;
+    static constexpr int Q_OFF = V_OFF + TILE;
+    static constexpr int DO_OFF = Q_OFF + QS * TILE;
+    static constexpr int DS_OFF = DO_OFF + QS * TILE;      // dS: two 64-query chunks (row = key)
+    static constexpr int DQ_OFF = DS_OFF + 2 * CHUNK_BYTES;  // dQ staging: two 32-column fp32 chunks
+    static constexpr int LSE_OFF = DQ_OFF + 2 * CHUNK_BYTES;
+    static constexpr int DD_OFF = LSE_OFF + QS * BM * 4;
+    static constexpr int BAR_OFF = DD_OFF + QS * BM * 4;
+    static constexpr int B_KVFULL = 0;
+    static constexpr int B_QFULL = 1;
+    static constexpr int B_QEMPTY = B_QFULL + QS;
+    static constexpr int B_SFULL = B_QEMPTY + QS;   // Sᵀ, dPᵀ computed                 (commit)
+    static constexpr int B_RDONE = B_SFULL + 1;     // Sᵀ, dPᵀ loaded by the softmax     (256 arrivals)
+    static constexpr int B_PFULL = B_RDONE + 1;     // Pᵀ and dS written                 (256 arrivals)
+    static constexpr int B_BDONE = B_PFULL + 1;     // dV, dK, dQ of the tile done       (commit)
+    static constexpr int B_DQFREE = B_BDONE + 1;    // dQ read out of tensor memory      (256 arrivals)
+    static constexpr int B_DKVDONE = B_DQFREE + 1;
+    static constexpr int B_EPI = B_DKVDONE + 1;     // epilogue staging steps            (256 arrivals)
+    static constexpr int B_NEVER = B_EPI + 1;
+    static constexpr int NBARS = B_NEVER + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int BYTES = MISC_OFF + 16 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 320, DQ_COL = 384, P_COL = 448;
+    static_assert(BYTES <= 232448, "shared memory budget");
+};
+
+template <int MASK>
+__global__ void __launch_bounds__(LayoutPipe::NUM_THREADS, 1)
+attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
+{
+    using L = LayoutPipe;
+    constexpr int D = 64;
+    const int kb = static_cast<int>(blockIdx.x) % p.num_kblocks;
+    const int bh = static_cast<int>(blockIdx.x) / p.num_kblocks;
+    const int k0 = kb * BN;
+    int kv_len = p.m;
+    if (mask_has_lengths(MASK)) {
+        const int len = __ldg(p.key_lengths + bh / p.H);
+        kv_len = len < 0 ? 0 : (len > p.m ? p.m : len);
+    }
+    if (k0 >= kv_len) {
+        // no query sees these keys: their gradients are zero
+        const int rows = min(BN, p.m - k0);
+        const int64_t base = (static_cast<int64_t>(bh) * p.m + k0) * D;
+        uint4* gk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dK) + base);
+        uint4* gv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dV) + base);
+        for (int i = threadIdx.x; i < rows * D / 8; i += blockDim.x) {
+            gk[i] = make_uint4(0u, 0u, 0u, 0u);
+            gv[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        return;
+    }
+    const int nqb = (p.n + BM - 1) / BM;
+    int qb_lo = 0;
+    if (mask_is_causal(MASK)) {
+        const int first_q = k0 - p.causal_off;     // first row that sees key k0
+        qb_lo = first_q <= 0 ? 0 : first_q / BM;
+    }
+    const int nt = nqb - qb_lo;                    // >= 1
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::BAR_OFF;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+    volatile uint32_t* abort_word = reinterpret_cast<volatile uint32_t*>(smem + L::MISC_OFF + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint64_t limit = p.watchdog_ns;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::B_KVFULL), 1);
+        for (int s = 0; s < L::QS; ++s) {
+            mbar_init(bar(L::B_QFULL + s), 1);
+            mbar_init(bar(L::B_QEMPTY + s), 1);
+        }
+        mbar_init(bar(L::B_SFULL), 1);
+        mbar_init(bar(L::B_RDONE), L::COMPUTE_THREADS);
+        mbar_init(bar(L::B_PFULL), L::COMPUTE_THREADS);
+        mbar_init(bar(L::B_BDONE), 1);
+        mbar_init(bar(L::B_DQFREE), L::COMPUTE_THREADS);
+        mbar_init(bar(L::B_DKVDONE), 1);
+        mbar_init(bar(L::B_EPI), L::COMPUTE_THREADS);
+        mbar_init(bar(L::B_NEVER), 1);
+        *abort_word = 0u;
+        fence_mbar_init();
+    }
+    if (warp == L::WARP_MMA) {
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == L::WARP_TMA && lane == 0) {
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.k);
+        tma_prefetch_desc(&maps.v);
+        tma_prefetch_desc(&maps.dout);
+        tma_prefetch_desc(&maps.dk);
+        tma_prefetch_desc(&maps.dv);
+        tma_prefetch_desc(&maps.dq_acc);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const uint32_t sK = sbase + L::K_OFF;
+    const uint32_t sV = sbase + L::V_OFF;
+    const uint32_t sQ = sbase + L::Q_OFF;
+    const uint32_t sdO = sbase + L::DO_OFF;
+    const uint32_t sdS = sbase + L::DS_OFF;
+    const uint32_t sdQ = sbase + L::DQ_OFF;
+
+    if (warp >= L::WARP_TMA) {
+        if (warp == L::WARP_TMA && lane == 0) {
+            // ================================================== TMA producer
+            mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
+            tma_load_3d(sK, &maps.k, bar(L::B_KVFULL), 0, k0, bh);
+            tma_load_3d(sV, &maps.v, bar(L::B_KVFULL), 0, k0, bh);
+            int issued = 0;
+            for (int t = 0; t < nt; ++t) {
+                const int s = t % L::QS;
+                if (t >= L::QS &&
+                    !mbar_wait(bar(L::B_QEMPTY + s), static_cast<uint32_t>(t / L::QS - 1) & 1u, abort_word,
+                               p.status, STATUS_TMA_WAIT, limit))
+                    break;
+                const int q0 = (qb_lo + t) * BM;
+                mbar_arrive_expect_tx(bar(L::B_QFULL + s), 2 * L::TILE + 2 * BM * 4);
+                tma_load_3d(sQ + s * L::TILE, &maps.q, bar(L::B_QFULL + s), 0, q0, bh);
+                tma_load_3d(sdO + s * L::TILE, &maps.dout, bar(L::B_QFULL + s), 0, q0, bh);
+                const int64_t row0 = static_cast<int64_t>(bh) * p.n_pad + q0;
+                bulk_load(sbase + L::LSE_OFF + s * BM * 4, p.lse2 + row0, BM * 4, bar(L::B_QFULL + s));
+                bulk_load(sbase + L::DD_OFF + s * BM * 4, p.dd + row0, BM * 4, bar(L::B_QFULL + s));
+                ++issued;
+            }
+            drain(bar(L::B_KVFULL), 0, 100000000ull);
+            for (int t = issued - 1; t >= 0 && t >= issued - L::QS; --t)
+                drain(bar(L::B_QFULL + t % L::QS), static_cast<uint32_t>(t / L::QS) & 1u, 100000000ull);
+        } else if (warp == L::WARP_MMA) {
+            // ================================================== MMA issuer (whole warp, one elected lane)
+            constexpr uint32_t ID_S = idesc_bf16_f32(BN, BM, false, false);   // M = keys, N = queries
+            constexpr uint32_t ID_KV = idesc_bf16_f32(BN, D, false, true);    // M = keys, N = d
+            constexpr uint32_t ID_DQ = idesc_bf16_f32(BM, D, true, true);     // M = queries, N = d
+            const uint64_t dK_k = sdesc_sw128(sK, 16, 1024);
+            const uint64_t dV_k = sdesc_sw128(sV, 16, 1024);
+            const uint64_t dK_mn = sdesc_sw128(sK, CHUNK_BYTES, 1024);
+            const uint64_t dS_mn = sdesc_sw128(sdS, CHUNK_BYTES, 1024);
+            const uint64_t dS_k = sdesc_sw128(sdS, 16, 1024);
+            auto wait = [&](int b, uint32_t parity) -> bool {
+                const bool r = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_MMA_WAIT, limit);
+                return __all_sync(0xffffffffu, r);
+            };
+            // Sᵀ = K Qᵀ and dPᵀ = V dOᵀ of tile t into their columns
+            auto issue_A = [&](int t) {
+                const int s = t % L::QS;
+                const uint64_t dQ_k = sdesc_sw128(sQ + s * L::TILE, 16, 1024);
+                const uint64_t dO_k = sdesc_sw128(sdO + s * L::TILE, 16, 1024);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                    mma_ss_warp(tmem + L::S_COL, dK_k + off, dQ_k + off, ID_S, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
+                    mma_ss_warp(tmem + L::DP_COL, dV_k + off, dO_k + off, ID_S, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_warp(bar(L::B_SFULL));
+            };
+            bool ok = wait(L::B_KVFULL, 0) && wait(L::B_QFULL, 0);
+            if (ok) {
+                tc_fence_after();
+                issue_A(0);
+            }
+            for (int t = 0; ok && t < nt; ++t) {
+                const int s = t % L::QS;
+                const uint32_t parity = static_cast<uint32_t>(t) & 1u;
+                if (t + 1 < nt) {
+                    // tile t+1's scores as soon as the softmax warps hold tile t's
+                    ok = wait(L::B_QFULL + (t + 1) % L::QS, static_cast<uint32_t>((t + 1) / L::QS) & 1u) &&
+                         wait(L::B_RDONE, parity);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_A(t + 1);
+                }
+                ok = wait(L::B_PFULL, parity);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dO_mn = sdesc_sw128(sdO + s * L::TILE, CHUNK_BYTES, 1024);
+                const uint64_t dQ_mn = sdesc_sw128(sQ + s * L::TILE, CHUNK_BYTES, 1024);
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
+                    mma_ts_warp(tmem + L::DV_COL, tmem + L::P_COL + kk * 8, dO_mn + off, ID_KV,
+                                (t > 0 || kk > 0) ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < BM / 16; ++kk) {
+                    const uint64_t aoff = static_cast<uint64_t>(((kk / 4) * CHUNK_BYTES + (kk % 4) * 32) >> 4);
+                    const uint64_t boff = static_cast<uint64_t>((kk * 2048) >> 4);
+                    mma_ss_warp(tmem + L::DK_COL, dS_k + aoff, dQ_mn + boff, ID_KV, (t > 0 || kk > 0) ? 1u : 0u);
+                }
+                // the previous tile's dQ must have left its columns
+                if (t > 0 && !wait(L::B_DQFREE, parity ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
+                    mma_ss_warp(tmem + L::DQ_COL, dS_mn + off, dK_mn + off, ID_DQ, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_warp(bar(L::B_BDONE));
+                mma_commit_warp(bar(L::B_QEMPTY + s));
+            }
+            mma_commit_warp(bar(L::B_DKVDONE));
+            drain(bar(L::B_DKVDONE), 0, 100000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ================================================== Pᵀ / dS, dQ read-out, epilogue
+        const int wq = warp % 4;                      // lane quadrant
+        const int half = warp / 4;                    // column half
+        const int r = 32 * wq + lane;                 // TMEM lane: a key here, a query row for dQ
+        const int key = k0 + r;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
+        const float sl2 = p.scale_log2;
+        bool ok = true;
+        bool dq_pending = false;     // this warp has a dQ reduce-add whose read may be pending
+        int epi_phase = 0;
+        auto rendezvous = [&](int b, uint32_t parity) -> bool {
+            mbar_arrive(bar(b));
+            const bool rr = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
+            return __all_sync(0xffffffffu, rr);
+        };
+
+        if (p.debug_flags & DEBUG_FORCE_TIMEOUT) {
+            ok = mbar_wait(bar(L::B_NEVER), 0, abort_word, p.status, STATUS_FORCED, 20000000ull);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        // dQ of tile tq (in tensor memory once B_BDONE of tq completed): this
+        // warpgroup's 32 columns -> its staging chunk -> TMA reduce-add
+        auto dq_out = [&](int tq) {
+            uint32_t a[32];
+            tmem_ld32(tmem + lane_base + L::DQ_COL + 32 * half, a);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(L::B_DQFREE));
+            if (dq_pending && lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+            const uint32_t row_base = sdQ + half * CHUNK_BYTES + r * 128;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t addr = row_base + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a[4 * q]),
+                             "r"(a[4 * q + 1]), "r"(a[4 * q + 2]), "r"(a[4 * q + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int q0 = (qb_lo + tq) * BM;
+            if (lane == 0 && q0 + 32 * wq < p.n) {
+                tma_reduce_add_3d(&maps.dq_acc, sdQ + half * CHUNK_BYTES + wq * 32 * 128, 32 * half, q0 + 32 * wq, bh);
+                bulk_commit_group();
+                dq_pending = true;
+            }
+            __syncwarp();
+        };
+
+        for (int t = 0; ok && t < nt; ++t) {
+            const int s = t % L::QS;
+            const uint32_t parity = static_cast<uint32_t>(t) & 1u;
+            const int q0 = (qb_lo + t) * BM;
+            ok = mbar_wait(bar(L::B_QFULL + s), static_cast<uint32_t>(t / L::QS) & 1u, abort_word, p.status,
+                           STATUS_SOFTMAX_WAIT, limit) &&
+                 mbar_wait(bar(L::B_SFULL), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const int c0 = 64 * half;                 // this warpgroup's first query column
+            uint32_t sr[64], dr[64];
+            tmem_ld32(tmem + lane_base + L::S_COL + c0, sr);
+            tmem_ld32(tmem + lane_base + L::S_COL + c0 + 32, sr + 32);
+            tmem_ld32(tmem + lane_base + L::DP_COL + c0, dr);
+            tmem_ld32(tmem + lane_base + L::DP_COL + c0 + 32, dr + 32);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(bar(L::B_RDONE));            // the MMA warp may compute the next Sᵀ, dPᵀ
+            const uint32_t lse_s = sbase + L::LSE_OFF + (s * BM + c0) * 4;
+            const uint32_t dd_s = sbase + L::DD_OFF + (s * BM + c0) * 4;
+            const bool need_mask =
+                __any_sync(0xffffffffu, key >= kv_len || q0 + c0 + 63 >= p.n ||
+                                            (mask_is_causal(MASK) && key > q0 + c0 + p.causal_off));
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float lz[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) lds_v4f(lse_s + (32 * c + 4 * v) * 4, lz + 4 * v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = 32 * c + i;
+                    sr[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, -lz[i])));
+                }
+            }
+            if (need_mask) {
+                const int q_first = key >= kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - p.causal_off : 0);
+                const int j_lo = q_first == INT32_MAX ? BM : max(q_first - q0, 0) - c0;
+                const int j_hi = min(p.n - q0, BM) - c0;
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    if (j < j_lo || j >= j_hi) sr[j] = 0u;
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float dz[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) lds_v4f(dd_s + (32 * c + 4 * v) * 4, dz + 4 * v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int j = 32 * c + i;
+                    dr[j] = __float_as_uint(__uint_as_float(sr[j]) * (__uint_as_float(dr[j]) - dz[i]));
+                }
+            }
+            // the previous tile's dV, dK, dQ have consumed Pᵀ and dS
+            if (t > 0) {
+                ok = mbar_wait(bar(L::B_BDONE), parity ^ 1u, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+            }
+            {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+                tmem_st32(tmem + lane_base + L::P_COL + 32 * half, pk);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
+                // dS: row = key r, chunk = this warpgroup's 64 queries
+                const uint32_t row_base = sdS + half * CHUNK_BYTES + r * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t addr = row_base + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * q]),
+                                 "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                                 : "memory");
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(L::B_PFULL));
+            if (t > 0) dq_out(t - 1);                 // waited for above (B_BDONE of t - 1)
+        }
+        if (ok) {
+            // the last tile's dQ
+            ok = mbar_wait(bar(L::B_BDONE), static_cast<uint32_t>(nt - 1) & 1u, abort_word, p.status,
+                           STATUS_SOFTMAX_WAIT, limit);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                tc_fence_after();
+                dq_out(nt - 1);
+            }
+        }
+
+        // ---------------------------------------- dV, then dK (x scale): TMEM -> bf16 staging -> TMA store
+        // The two warpgroups convert 32 columns each into one 64-column staging chunk
+        // (the dS area, free once every MMA is done); warpgroup 0 stores it.
+        if (ok) {
+            ok = mbar_wait(bar(L::B_DKVDONE), 0, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        bool st_pending = false;
+        if (ok) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t col = which == 0 ? L::DV_COL : L::DK_COL;
+                const float mul = which == 0 ? 1.f : p.scale;
+                if (st_pending && lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+                ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
+                if (!ok) break;
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_base + col + 32 * half, o);
+                tmem_wait_ld();
+                const uint32_t chunk_base = sdS + r * 128;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        v[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * mul,
+                                           __uint_as_float(o[8 * q + 2 * e + 1]) * mul);
+                    const uint32_t piece = static_cast<uint32_t>(half * 4 + q);
+                    const uint32_t addr = chunk_base + ((piece ^ static_cast<uint32_t>(r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
+                                 "r"(v[2]), "r"(v[3])
+                                 : "memory");
+                }
+                fence_proxy_async_smem();
+                ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
+                if (!ok) break;
+                if (half == 0 && lane == 0 && k0 + 32 * wq < p.m) {
+                    tma_store_3d(which == 0 ? &maps.dv : &maps.dk, sdS + wq * 32 * 128, 0, k0 + 32 * wq, bh);
+                    bulk_commit_group();
+                    st_pending = true;
                 }
                 __syncwarp();
             }
@@ -483,8 +961,8 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 template <int D, int MASK>
 cudaError_t launch(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream)
 {
-    using L = Layout<D>;
-    auto kern = attn_bwd_kernel<D, MASK>;
+    using L = typename std::conditional<D == 64, LayoutPipe, Layout<D>>::type;
+    auto kern = D == 64 ? attn_bwd_pipe_kernel<MASK> : attn_bwd_kernel<D, MASK>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
