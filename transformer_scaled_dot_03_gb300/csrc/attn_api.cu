@@ -553,6 +553,7 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
     p.m = m;
     p.causal_off = m - n;
     p.num_kblocks = static_cast<int>((static_cast<int64_t>(m) + 127) / 128);
+    if ((rc = sm_count(&p.num_sms)) != ATTN_OK) return rc;
     p.n_pad = static_cast<int>(ws.n_pad);
     p.key_lengths = attn::mask_has_lengths(mask_kind) ? key_lengths : nullptr;
     p.lse2 = lse2;

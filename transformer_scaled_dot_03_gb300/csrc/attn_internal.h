@@ -61,6 +61,7 @@ struct BwdParams {
     int causal_off;               // m - n
     int num_kblocks;              // ceil(m / 128)
     int n_pad;                    // query rows padded to whole tiles (lse2 / dd row stride)
+    int num_sms;                  // sizes the persistent grid (d = 64)
     const int32_t* key_lengths;   // device int32 [B] (key-padding masks only)
     const float* lse2;            // [B*H, n_pad]: LSE * log2(e), 0 in the padding
     const float* dd;              // [B*H, n_pad]: D = rowsum(dO * O), 0 in the padding

@@ -510,16 +510,25 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 }
 
 // ---------------------------------------------------------------------------
-// d = 64: the same computation with the query tiles pipelined. dK += dSᵀ Q takes
-// dS from shared memory (the tile written for dQ, row = key with the queries
-// contiguous, is exactly the K-major layout of A = dSᵀ), so dSᵀ needs no tensor
-// memory and Pᵀ gets columns of its own. Then nothing the MMAs of tile t read
-// overlaps what Sᵀ and dPᵀ of tile t+1 write, and the MMA warp issues
-//     Sᵀ, dPᵀ (t+1)   as soon as the softmax warps have loaded Sᵀ, dPᵀ (t)
+// d = 64: the same computation, persistent and with the query tiles pipelined.
+//
+// dK += dSᵀ Q takes dS from shared memory (the tile written for dQ, row = key with
+// the queries contiguous, is exactly the K-major layout of A = dSᵀ), so dSᵀ needs
+// no tensor memory and Pᵀ gets columns of its own. Then nothing the MMAs of tile t
+// read overlaps what Sᵀ and dPᵀ of the next tile write, and the MMA warp issues
+//     Sᵀ, dPᵀ (next)  as soon as the softmax warps have loaded Sᵀ, dPᵀ (t)
 //     dV, dK, dQ (t)  once Pᵀ (t) and dS (t) are written,
-// so the tensor cores compute tile t+1's scores while the softmax warps turn tile
-// t's into Pᵀ and dS. The dQ of tile t is read out one iteration later (after
-// tile t+1's Pᵀ and dS), through a staging area of its own.
+// so the tensor cores compute the next tile's scores while the softmax warps turn
+// tile t's into Pᵀ and dS. The dQ of a tile is read out one iteration later,
+// through a staging area of its own.
+//
+// Persistent: one CTA per SM walks work items (b, h, 128-key tile) round-robin;
+// under the causal masks a unit pairs key tile k with key tile nkb-1-k of the same
+// head (the one with most query tiles with the one with fewest), so that units
+// cost the same. K and V are double-buffered, so the next item's keys load during
+// the current item's last tiles, and its first scores are computed while the
+// softmax warps write the current item's dK and dV out. Barrier phases run on
+// per-CTA tile and item counters.
 //   Tensor memory: Sᵀ [0,128), dPᵀ [128,256), dV [256,320), dK [320,384),
 //   dQ [384,448), Pᵀ [448,512).
 struct LayoutPipe {
@@ -529,10 +538,11 @@ struct LayoutPipe {
     static constexpr int COMPUTE_THREADS = 256;
     static constexpr int WARP_TMA = 8;
     static constexpr int WARP_MMA = 9;
-    static constexpr int QS = 2;
+    static constexpr int QS = 2;                             // Q/dO/LSE/D ring depth
+    static constexpr int KVS = 2;                            // K/V buffers
     static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + TILE;
-    static constexpr int Q_OFF = V_OFF + TILE;
+    static constexpr int V_OFF = K_OFF + KVS * TILE;
+    static constexpr int Q_OFF = V_OFF + KVS * TILE;
     static constexpr int DO_OFF = Q_OFF + QS * TILE;
     static constexpr int DS_OFF = DO_OFF + QS * TILE;      // dS: two 64-query chunks (row = key)
     static constexpr int DQ_OFF = DS_OFF + 2 * CHUNK_BYTES;  // dQ staging: two 32-column fp32 chunks
@@ -540,16 +550,19 @@ struct LayoutPipe {
     static constexpr int DD_OFF = LSE_OFF + QS * BM * 4;
     static constexpr int BAR_OFF = DD_OFF + QS * BM * 4;
     static constexpr int B_KVFULL = 0;
-    static constexpr int B_QFULL = 1;
+    static constexpr int B_KVEMPTY = B_KVFULL + KVS;
+    static constexpr int B_QFULL = B_KVEMPTY + KVS;
     static constexpr int B_QEMPTY = B_QFULL + QS;
     static constexpr int B_SFULL = B_QEMPTY + QS;   // Sᵀ, dPᵀ computed                 (commit)
     static constexpr int B_RDONE = B_SFULL + 1;     // Sᵀ, dPᵀ loaded by the softmax     (256 arrivals)
     static constexpr int B_PFULL = B_RDONE + 1;     // Pᵀ and dS written                 (256 arrivals)
     static constexpr int B_BDONE = B_PFULL + 1;     // dV, dK, dQ of the tile done       (commit)
     static constexpr int B_DQFREE = B_BDONE + 1;    // dQ read out of tensor memory      (256 arrivals)
-    static constexpr int B_DKVDONE = B_DQFREE + 1;
-    static constexpr int B_EPI = B_DKVDONE + 1;     // epilogue staging steps            (256 arrivals)
-    static constexpr int B_NEVER = B_EPI + 1;
+    static constexpr int B_DKVDONE = B_DQFREE + 1;  // an item's dV, dK complete         (commit)
+    static constexpr int B_DKVFREE = B_DKVDONE + 1; // an item's dV, dK read out         (256 arrivals)
+    static constexpr int B_EPI = B_DKVFREE + 1;     // epilogue staging steps            (256 arrivals)
+    static constexpr int B_DRAIN = B_EPI + 1;
+    static constexpr int B_NEVER = B_DRAIN + 1;
     static constexpr int NBARS = B_NEVER + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16 + 1024;
@@ -558,39 +571,92 @@ struct LayoutPipe {
     static_assert(BYTES <= 232448, "shared memory budget");
 };
 
+// One work item: a 128-key tile of one (b, h) pair and the query tiles that see it.
+struct BwdItem {
+    int bh, k0, kv_len, qb_lo, nt;   // nt = 0: no query sees these keys (zero gradients)
+};
+
+template <int MASK>
+__device__ __forceinline__ int bwd_units_per_head(const BwdParams& p)
+{
+    return mask_is_causal(MASK) ? (p.num_kblocks + 1) / 2 : p.num_kblocks;
+}
+
+template <int MASK>
+__device__ __forceinline__ int bwd_items_of_unit(int u, const BwdParams& p)
+{
+    if (!mask_is_causal(MASK)) return 1;
+    const int k = u % bwd_units_per_head<MASK>(p);
+    return (k == p.num_kblocks - 1 - k) ? 1 : 2;
+}
+
+template <int MASK>
+__device__ __forceinline__ BwdItem bwd_item(int u, int iu, const BwdParams& p)
+{
+    const int uph = bwd_units_per_head<MASK>(p);
+    BwdItem w;
+    w.bh = u / uph;
+    const int k = u % uph;
+    const int kb = (mask_is_causal(MASK) && iu == 1) ? p.num_kblocks - 1 - k : k;
+    w.k0 = kb * BN;
+    w.kv_len = p.m;
+    if (mask_has_lengths(MASK)) {
+        const int len = __ldg(p.key_lengths + w.bh / p.H);
+        w.kv_len = len < 0 ? 0 : (len > p.m ? p.m : len);
+    }
+    w.qb_lo = 0;
+    if (mask_is_causal(MASK)) {
+        const int first_q = w.k0 - p.causal_off;     // first row that sees key k0
+        w.qb_lo = first_q <= 0 ? 0 : first_q / BM;
+    }
+    const int nqb = (p.n + BM - 1) / BM;
+    w.nt = w.k0 >= w.kv_len ? 0 : nqb - w.qb_lo;
+    return w;
+}
+
+// Walks the tiles of this CTA's items in order, skipping items without queries.
+template <int MASK>
+struct BwdCursor {
+    int u, iu, t;
+    BwdItem w;
+    bool valid;
+    __device__ void settle(const BwdParams& p, int num_units)
+    {
+        while (u < num_units) {
+            w = bwd_item<MASK>(u, iu, p);
+            if (t < w.nt) {
+                valid = true;
+                return;
+            }
+            t = 0;
+            if (++iu >= bwd_items_of_unit<MASK>(u, p)) {
+                iu = 0;
+                u += static_cast<int>(gridDim.x);
+            }
+        }
+        valid = false;
+    }
+    __device__ void start(const BwdParams& p, int num_units)
+    {
+        u = static_cast<int>(blockIdx.x);
+        iu = 0;
+        t = 0;
+        settle(p, num_units);
+    }
+    __device__ void next(const BwdParams& p, int num_units)
+    {
+        ++t;
+        settle(p, num_units);
+    }
+};
+
 template <int MASK>
 __global__ void __launch_bounds__(LayoutPipe::NUM_THREADS, 1)
 attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 {
     using L = LayoutPipe;
     constexpr int D = 64;
-    const int kb = static_cast<int>(blockIdx.x) % p.num_kblocks;
-    const int bh = static_cast<int>(blockIdx.x) / p.num_kblocks;
-    const int k0 = kb * BN;
-    int kv_len = p.m;
-    if (mask_has_lengths(MASK)) {
-        const int len = __ldg(p.key_lengths + bh / p.H);
-        kv_len = len < 0 ? 0 : (len > p.m ? p.m : len);
-    }
-    if (k0 >= kv_len) {
-        // no query sees these keys: their gradients are zero
-        const int rows = min(BN, p.m - k0);
-        const int64_t base = (static_cast<int64_t>(bh) * p.m + k0) * D;
-        uint4* gk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dK) + base);
-        uint4* gv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dV) + base);
-        for (int i = threadIdx.x; i < rows * D / 8; i += blockDim.x) {
-            gk[i] = make_uint4(0u, 0u, 0u, 0u);
-            gv[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        return;
-    }
-    const int nqb = (p.n + BM - 1) / BM;
-    int qb_lo = 0;
-    if (mask_is_causal(MASK)) {
-        const int first_q = k0 - p.causal_off;     // first row that sees key k0
-        qb_lo = first_q <= 0 ? 0 : first_q / BM;
-    }
-    const int nt = nqb - qb_lo;                    // >= 1
+    const int num_units = p.B * p.H * bwd_units_per_head<MASK>(p);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -605,7 +671,10 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     const uint64_t limit = p.watchdog_ns;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::B_KVFULL), 1);
+        for (int s = 0; s < L::KVS; ++s) {
+            mbar_init(bar(L::B_KVFULL + s), 1);
+            mbar_init(bar(L::B_KVEMPTY + s), 1);
+        }
         for (int s = 0; s < L::QS; ++s) {
             mbar_init(bar(L::B_QFULL + s), 1);
             mbar_init(bar(L::B_QEMPTY + s), 1);
@@ -616,7 +685,9 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         mbar_init(bar(L::B_BDONE), 1);
         mbar_init(bar(L::B_DQFREE), L::COMPUTE_THREADS);
         mbar_init(bar(L::B_DKVDONE), 1);
+        mbar_init(bar(L::B_DKVFREE), L::COMPUTE_THREADS);
         mbar_init(bar(L::B_EPI), L::COMPUTE_THREADS);
+        mbar_init(bar(L::B_DRAIN), 1);
         mbar_init(bar(L::B_NEVER), 1);
         *abort_word = 0u;
         fence_mbar_init();
@@ -649,47 +720,65 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     if (warp >= L::WARP_TMA) {
         if (warp == L::WARP_TMA && lane == 0) {
             // ================================================== TMA producer
-            mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
-            tma_load_3d(sK, &maps.k, bar(L::B_KVFULL), 0, k0, bh);
-            tma_load_3d(sV, &maps.v, bar(L::B_KVFULL), 0, k0, bh);
-            int issued = 0;
-            for (int t = 0; t < nt; ++t) {
-                const int s = t % L::QS;
-                if (t >= L::QS &&
-                    !mbar_wait(bar(L::B_QEMPTY + s), static_cast<uint32_t>(t / L::QS - 1) & 1u, abort_word,
-                               p.status, STATUS_TMA_WAIT, limit))
+            BwdCursor<MASK> cur;
+            cur.start(p, num_units);
+            int gt = 0, it = 0;          // tiles and items so far
+            int kv_issued = 0;           // K/V loads issued
+            bool ok = true;
+            while (ok && cur.valid) {
+                if (cur.t == 0) {
+                    const int ks = it % L::KVS;
+                    if (it >= L::KVS &&
+                        !mbar_wait(bar(L::B_KVEMPTY + ks), static_cast<uint32_t>(it / L::KVS - 1) & 1u, abort_word,
+                                   p.status, STATUS_TMA_WAIT, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(L::B_KVFULL + ks), 2 * L::TILE);
+                    tma_load_3d(sK + ks * L::TILE, &maps.k, bar(L::B_KVFULL + ks), 0, cur.w.k0, cur.w.bh);
+                    tma_load_3d(sV + ks * L::TILE, &maps.v, bar(L::B_KVFULL + ks), 0, cur.w.k0, cur.w.bh);
+                    ++kv_issued;
+                }
+                const int s = gt % L::QS;
+                if (gt >= L::QS &&
+                    !mbar_wait(bar(L::B_QEMPTY + s), static_cast<uint32_t>(gt / L::QS - 1) & 1u, abort_word,
+                               p.status, STATUS_TMA_WAIT, limit)) {
+                    ok = false;
                     break;
-                const int q0 = (qb_lo + t) * BM;
+                }
+                const int q0 = (cur.w.qb_lo + cur.t) * BM;
                 mbar_arrive_expect_tx(bar(L::B_QFULL + s), 2 * L::TILE + 2 * BM * 4);
-                tma_load_3d(sQ + s * L::TILE, &maps.q, bar(L::B_QFULL + s), 0, q0, bh);
-                tma_load_3d(sdO + s * L::TILE, &maps.dout, bar(L::B_QFULL + s), 0, q0, bh);
-                const int64_t row0 = static_cast<int64_t>(bh) * p.n_pad + q0;
+                tma_load_3d(sQ + s * L::TILE, &maps.q, bar(L::B_QFULL + s), 0, q0, cur.w.bh);
+                tma_load_3d(sdO + s * L::TILE, &maps.dout, bar(L::B_QFULL + s), 0, q0, cur.w.bh);
+                const int64_t row0 = static_cast<int64_t>(cur.w.bh) * p.n_pad + q0;
                 bulk_load(sbase + L::LSE_OFF + s * BM * 4, p.lse2 + row0, BM * 4, bar(L::B_QFULL + s));
                 bulk_load(sbase + L::DD_OFF + s * BM * 4, p.dd + row0, BM * 4, bar(L::B_QFULL + s));
-                ++issued;
+                if (cur.t == cur.w.nt - 1) ++it;
+                ++gt;
+                cur.next(p, num_units);
             }
-            drain(bar(L::B_KVFULL), 0, 100000000ull);
-            for (int t = issued - 1; t >= 0 && t >= issued - L::QS; --t)
-                drain(bar(L::B_QFULL + t % L::QS), static_cast<uint32_t>(t / L::QS) & 1u, 100000000ull);
+            // land every copy still in flight (only possible after an abort)
+            for (int i = kv_issued - 1; i >= 0 && i >= kv_issued - L::KVS; --i)
+                drain(bar(L::B_KVFULL + i % L::KVS), static_cast<uint32_t>(i / L::KVS) & 1u, 100000000ull);
+            for (int i = gt - 1; i >= 0 && i >= gt - L::QS; --i)
+                drain(bar(L::B_QFULL + i % L::QS), static_cast<uint32_t>(i / L::QS) & 1u, 100000000ull);
         } else if (warp == L::WARP_MMA) {
             // ================================================== MMA issuer (whole warp, one elected lane)
             constexpr uint32_t ID_S = idesc_bf16_f32(BN, BM, false, false);   // M = keys, N = queries
             constexpr uint32_t ID_KV = idesc_bf16_f32(BN, D, false, true);    // M = keys, N = d
             constexpr uint32_t ID_DQ = idesc_bf16_f32(BM, D, true, true);     // M = queries, N = d
-            const uint64_t dK_k = sdesc_sw128(sK, 16, 1024);
-            const uint64_t dV_k = sdesc_sw128(sV, 16, 1024);
-            const uint64_t dK_mn = sdesc_sw128(sK, CHUNK_BYTES, 1024);
             const uint64_t dS_mn = sdesc_sw128(sdS, CHUNK_BYTES, 1024);
             const uint64_t dS_k = sdesc_sw128(sdS, 16, 1024);
             auto wait = [&](int b, uint32_t parity) -> bool {
                 const bool r = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_MMA_WAIT, limit);
                 return __all_sync(0xffffffffu, r);
             };
-            // Sᵀ = K Qᵀ and dPᵀ = V dOᵀ of tile t into their columns
-            auto issue_A = [&](int t) {
-                const int s = t % L::QS;
-                const uint64_t dQ_k = sdesc_sw128(sQ + s * L::TILE, 16, 1024);
-                const uint64_t dO_k = sdesc_sw128(sdO + s * L::TILE, 16, 1024);
+            // Sᵀ = K Qᵀ and dPᵀ = V dOᵀ of the tile in Q buffer qs, keys in K/V buffer ks
+            auto issue_A = [&](int qs, int ks) {
+                const uint64_t dK_k = sdesc_sw128(sK + ks * L::TILE, 16, 1024);
+                const uint64_t dV_k = sdesc_sw128(sV + ks * L::TILE, 16, 1024);
+                const uint64_t dQ_k = sdesc_sw128(sQ + qs * L::TILE, 16, 1024);
+                const uint64_t dO_k = sdesc_sw128(sdO + qs * L::TILE, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>((kk * 32) >> 4);
@@ -702,41 +791,57 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 }
                 mma_commit_warp(bar(L::B_SFULL));
             };
-            bool ok = wait(L::B_KVFULL, 0) && wait(L::B_QFULL, 0);
-            if (ok) {
-                tc_fence_after();
-                issue_A(0);
+            BwdCursor<MASK> cur;
+            cur.start(p, num_units);
+            bool ok = true;
+            int gt = 0, it = 0;
+            if (cur.valid) {
+                ok = wait(L::B_KVFULL, 0) && wait(L::B_QFULL, 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_A(0, 0);
+                }
             }
-            for (int t = 0; ok && t < nt; ++t) {
-                const int s = t % L::QS;
-                const uint32_t parity = static_cast<uint32_t>(t) & 1u;
-                if (t + 1 < nt) {
-                    // tile t+1's scores as soon as the softmax warps hold tile t's
-                    ok = wait(L::B_QFULL + (t + 1) % L::QS, static_cast<uint32_t>((t + 1) / L::QS) & 1u) &&
+            while (ok && cur.valid) {
+                const int s = gt % L::QS;
+                const int ks = it % L::KVS;
+                const uint32_t parity = static_cast<uint32_t>(gt) & 1u;
+                BwdCursor<MASK> nx = cur;
+                nx.next(p, num_units);
+                if (nx.valid) {
+                    // the next tile's scores as soon as the softmax warps hold this tile's
+                    const bool new_item = nx.t == 0;
+                    const int nks = (it + (new_item ? 1 : 0)) % L::KVS;
+                    ok = wait(L::B_QFULL + (gt + 1) % L::QS, static_cast<uint32_t>((gt + 1) / L::QS) & 1u) &&
+                         (!new_item || wait(L::B_KVFULL + nks, static_cast<uint32_t>((it + 1) / L::KVS) & 1u)) &&
                          wait(L::B_RDONE, parity);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_A(t + 1);
+                    issue_A((gt + 1) % L::QS, nks);
                 }
                 ok = wait(L::B_PFULL, parity);
+                // this item's first dV, dK overwrite the accumulators of the previous item
+                if (ok && cur.t == 0 && it > 0) ok = wait(L::B_DKVFREE, static_cast<uint32_t>(it - 1) & 1u);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t dO_mn = sdesc_sw128(sdO + s * L::TILE, CHUNK_BYTES, 1024);
                 const uint64_t dQ_mn = sdesc_sw128(sQ + s * L::TILE, CHUNK_BYTES, 1024);
+                const uint64_t dK_mn = sdesc_sw128(sK + ks * L::TILE, CHUNK_BYTES, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
                     mma_ts_warp(tmem + L::DV_COL, tmem + L::P_COL + kk * 8, dO_mn + off, ID_KV,
-                                (t > 0 || kk > 0) ? 1u : 0u);
+                                (cur.t > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk) {
                     const uint64_t aoff = static_cast<uint64_t>(((kk / 4) * CHUNK_BYTES + (kk % 4) * 32) >> 4);
                     const uint64_t boff = static_cast<uint64_t>((kk * 2048) >> 4);
-                    mma_ss_warp(tmem + L::DK_COL, dS_k + aoff, dQ_mn + boff, ID_KV, (t > 0 || kk > 0) ? 1u : 0u);
+                    mma_ss_warp(tmem + L::DK_COL, dS_k + aoff, dQ_mn + boff, ID_KV,
+                                (cur.t > 0 || kk > 0) ? 1u : 0u);
                 }
                 // the previous tile's dQ must have left its columns
-                if (t > 0 && !wait(L::B_DQFREE, parity ^ 1u)) {
+                if (gt > 0 && !wait(L::B_DQFREE, parity ^ 1u)) {
                     ok = false;
                     break;
                 }
@@ -748,9 +853,16 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 }
                 mma_commit_warp(bar(L::B_BDONE));
                 mma_commit_warp(bar(L::B_QEMPTY + s));
+                if (cur.t == cur.w.nt - 1) {
+                    mma_commit_warp(bar(L::B_DKVDONE));
+                    mma_commit_warp(bar(L::B_KVEMPTY + ks));
+                    ++it;
+                }
+                ++gt;
+                cur = nx;
             }
-            mma_commit_warp(bar(L::B_DKVDONE));
-            drain(bar(L::B_DKVDONE), 0, 100000000ull);
+            mma_commit_warp(bar(L::B_DRAIN));
+            drain(bar(L::B_DRAIN), 0, 100000000ull);
         }
         __syncwarp();
     } else {
@@ -758,32 +870,37 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         const int wq = warp % 4;                      // lane quadrant
         const int half = warp / 4;                    // column half
         const int r = 32 * wq + lane;                 // TMEM lane: a key here, a query row for dQ
-        const int key = k0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
         const float sl2 = p.scale_log2;
         bool ok = true;
-        bool dq_pending = false;     // this warp has a dQ reduce-add whose read may be pending
+        bool bulk_pending = false;   // this warp has committed bulk groups (reduce-adds, stores)
         int epi_phase = 0;
+        int gt = 0, it = 0;
+        int prev_q0 = 0, prev_bh = 0;
+        bool has_prev = false;       // a tile whose dQ is still to be read out
         auto rendezvous = [&](int b, uint32_t parity) -> bool {
             mbar_arrive(bar(b));
             const bool rr = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
             return __all_sync(0xffffffffu, rr);
+        };
+        auto wait_bulk_read = [&]() {
+            if (bulk_pending && lane == 0) bulk_wait_group_read0();
+            __syncwarp();
         };
 
         if (p.debug_flags & DEBUG_FORCE_TIMEOUT) {
             ok = mbar_wait(bar(L::B_NEVER), 0, abort_word, p.status, STATUS_FORCED, 20000000ull);
             ok = __all_sync(0xffffffffu, ok);
         }
-        // dQ of tile tq (in tensor memory once B_BDONE of tq completed): this
+        // dQ of the previous tile (in tensor memory once its B_BDONE completed): this
         // warpgroup's 32 columns -> its staging chunk -> TMA reduce-add
-        auto dq_out = [&](int tq) {
+        auto dq_out = [&]() {
             uint32_t a[32];
             tmem_ld32(tmem + lane_base + L::DQ_COL + 32 * half, a);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(bar(L::B_DQFREE));
-            if (dq_pending && lane == 0) bulk_wait_group_read0();
-            __syncwarp();
+            wait_bulk_read();
             const uint32_t row_base = sdQ + half * CHUNK_BYTES + r * 128;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
@@ -794,156 +911,193 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             }
             fence_proxy_async_smem();
             __syncwarp();
-            const int q0 = (qb_lo + tq) * BM;
-            if (lane == 0 && q0 + 32 * wq < p.n) {
-                tma_reduce_add_3d(&maps.dq_acc, sdQ + half * CHUNK_BYTES + wq * 32 * 128, 32 * half, q0 + 32 * wq, bh);
+            if (lane == 0 && prev_q0 + 32 * wq < p.n) {
+                tma_reduce_add_3d(&maps.dq_acc, sdQ + half * CHUNK_BYTES + wq * 32 * 128, 32 * half,
+                                  prev_q0 + 32 * wq, prev_bh);
                 bulk_commit_group();
-                dq_pending = true;
+                bulk_pending = true;
             }
             __syncwarp();
+            has_prev = false;
         };
 
-        for (int t = 0; ok && t < nt; ++t) {
-            const int s = t % L::QS;
-            const uint32_t parity = static_cast<uint32_t>(t) & 1u;
-            const int q0 = (qb_lo + t) * BM;
-            ok = mbar_wait(bar(L::B_QFULL + s), static_cast<uint32_t>(t / L::QS) & 1u, abort_word, p.status,
-                           STATUS_SOFTMAX_WAIT, limit) &&
-                 mbar_wait(bar(L::B_SFULL), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            const int c0 = 64 * half;                 // this warpgroup's first query column
-            uint32_t sr[64], dr[64];
-            tmem_ld32(tmem + lane_base + L::S_COL + c0, sr);
-            tmem_ld32(tmem + lane_base + L::S_COL + c0 + 32, sr + 32);
-            tmem_ld32(tmem + lane_base + L::DP_COL + c0, dr);
-            tmem_ld32(tmem + lane_base + L::DP_COL + c0 + 32, dr + 32);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(L::B_RDONE));            // the MMA warp may compute the next Sᵀ, dPᵀ
-            const uint32_t lse_s = sbase + L::LSE_OFF + (s * BM + c0) * 4;
-            const uint32_t dd_s = sbase + L::DD_OFF + (s * BM + c0) * 4;
-            const bool need_mask =
-                __any_sync(0xffffffffu, key >= kv_len || q0 + c0 + 63 >= p.n ||
-                                            (mask_is_causal(MASK) && key > q0 + c0 + p.causal_off));
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float lz[32];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) lds_v4f(lse_s + (32 * c + 4 * v) * 4, lz + 4 * v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = 32 * c + i;
-                    sr[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, -lz[i])));
+        for (int u = static_cast<int>(blockIdx.x); ok && u < num_units; u += static_cast<int>(gridDim.x)) {
+            const int n_items = bwd_items_of_unit<MASK>(u, p);
+            for (int iu = 0; ok && iu < n_items; ++iu) {
+                const BwdItem w = bwd_item<MASK>(u, iu, p);
+                if (w.nt == 0) {
+                    // no query sees these keys: their gradients are zero
+                    if (w.k0 < p.m) {
+                        const int rows = min(BN, p.m - w.k0);
+                        const int64_t base = (static_cast<int64_t>(w.bh) * p.m + w.k0) * D;
+                        uint4* gk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dK) + base);
+                        uint4* gv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dV) + base);
+                        for (int i = threadIdx.x; i < rows * D / 8; i += L::COMPUTE_THREADS) {
+                            gk[i] = make_uint4(0u, 0u, 0u, 0u);
+                            gv[i] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    continue;
                 }
-            }
-            if (need_mask) {
-                const int q_first = key >= kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - p.causal_off : 0);
-                const int j_lo = q_first == INT32_MAX ? BM : max(q_first - q0, 0) - c0;
-                const int j_hi = min(p.n - q0, BM) - c0;
+                const int key = w.k0 + r;
+                for (int t = 0; ok && t < w.nt; ++t) {
+                    const int s = gt % L::QS;
+                    const uint32_t parity = static_cast<uint32_t>(gt) & 1u;
+                    const int q0 = (w.qb_lo + t) * BM;
+                    ok = mbar_wait(bar(L::B_QFULL + s), static_cast<uint32_t>(gt / L::QS) & 1u, abort_word, p.status,
+                                   STATUS_SOFTMAX_WAIT, limit) &&
+                         mbar_wait(bar(L::B_SFULL), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int c0 = 64 * half;         // this warpgroup's first query column
+                    uint32_t sr[64], dr[64];
+                    tmem_ld32(tmem + lane_base + L::S_COL + c0, sr);
+                    tmem_ld32(tmem + lane_base + L::S_COL + c0 + 32, sr + 32);
+                    tmem_ld32(tmem + lane_base + L::DP_COL + c0, dr);
+                    tmem_ld32(tmem + lane_base + L::DP_COL + c0 + 32, dr + 32);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(bar(L::B_RDONE));    // the MMA warp may compute the next Sᵀ, dPᵀ
+                    const uint32_t lse_s = sbase + L::LSE_OFF + (s * BM + c0) * 4;
+                    const uint32_t dd_s = sbase + L::DD_OFF + (s * BM + c0) * 4;
+                    const bool need_mask =
+                        __any_sync(0xffffffffu, key >= w.kv_len || q0 + c0 + 63 >= p.n ||
+                                                    (mask_is_causal(MASK) && key > q0 + c0 + p.causal_off));
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    if (j < j_lo || j >= j_hi) sr[j] = 0u;
-            }
+                    for (int c = 0; c < 2; ++c) {
+                        float lz[32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                float dz[32];
+                        for (int v = 0; v < 8; ++v) lds_v4f(lse_s + (32 * c + 4 * v) * 4, lz + 4 * v);
 #pragma unroll
-                for (int v = 0; v < 8; ++v) lds_v4f(dd_s + (32 * c + 4 * v) * 4, dz + 4 * v);
+                        for (int i = 0; i < 32; ++i) {
+                            const int j = 32 * c + i;
+                            sr[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, -lz[i])));
+                        }
+                    }
+                    if (need_mask) {
+                        const int q_first =
+                            key >= w.kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - p.causal_off : 0);
+                        const int j_lo = q_first == INT32_MAX ? BM : max(q_first - q0, 0) - c0;
+                        const int j_hi = min(p.n - q0, BM) - c0;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int j = 32 * c + i;
-                    dr[j] = __float_as_uint(__uint_as_float(sr[j]) * (__uint_as_float(dr[j]) - dz[i]));
+                        for (int j = 0; j < 64; ++j)
+                            if (j < j_lo || j >= j_hi) sr[j] = 0u;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        float dz[32];
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) lds_v4f(dd_s + (32 * c + 4 * v) * 4, dz + 4 * v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int j = 32 * c + i;
+                            dr[j] = __float_as_uint(__uint_as_float(sr[j]) * (__uint_as_float(dr[j]) - dz[i]));
+                        }
+                    }
+                    // the previous tile's dV, dK, dQ have consumed Pᵀ and dS
+                    if (gt > 0) {
+                        ok = mbar_wait(bar(L::B_BDONE), parity ^ 1u, abort_word, p.status, STATUS_SOFTMAX_WAIT,
+                                       limit);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    {
+                        uint32_t pk[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+                        tmem_st32(tmem + lane_base + L::P_COL + 32 * half, pk);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            pk[i] = pack_bf16x2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
+                        // an epilogue store may still be reading this warp's rows of the dS area
+                        wait_bulk_read();
+                        const uint32_t row_base = sdS + half * CHUNK_BYTES + r * 128;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const uint32_t addr =
+                                row_base + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * q]),
+                                         "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                                         : "memory");
+                        }
+                    }
+                    tmem_wait_st();
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(bar(L::B_PFULL));
+                    if (has_prev) dq_out();           // B_BDONE of the previous tile was waited for above
+                    prev_q0 = q0;
+                    prev_bh = w.bh;
+                    has_prev = true;
+                    ++gt;
                 }
-            }
-            // the previous tile's dV, dK, dQ have consumed Pᵀ and dS
-            if (t > 0) {
-                ok = mbar_wait(bar(L::B_BDONE), parity ^ 1u, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
+                if (!ok) break;
+
+                // ---------------------------------------- this item's dV, then dK (x scale)
+                // Both are read out of tensor memory first (the next item's first dV, dK
+                // may then overwrite them); the two warpgroups convert 32 columns each into
+                // one 64-column staging chunk (in the dS area) and warpgroup 0 stores it.
+                ok = mbar_wait(bar(L::B_DKVDONE), static_cast<uint32_t>(it) & 1u, abort_word, p.status,
+                               STATUS_SOFTMAX_WAIT, limit);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-            }
-            {
-                uint32_t pk[32];
+                uint32_t ov[32], ok_[32];
+                tmem_ld32(tmem + lane_base + L::DV_COL + 32 * half, ov);
+                tmem_ld32(tmem + lane_base + L::DK_COL + 32 * half, ok_);
+                tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(L::B_DKVFREE));
+#pragma unroll 1
+                for (int which = 0; which < 2; ++which) {
+                    const uint32_t* o = which == 0 ? ov : ok_;
+                    const float mul = which == 0 ? 1.f : p.scale;
+                    wait_bulk_read();
+                    // both warpgroups' earlier stores have read the staging rows
+                    ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
+                    if (!ok) break;
+                    const uint32_t chunk_base = sdS + r * 128;
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
-                tmem_st32(tmem + lane_base + L::P_COL + 32 * half, pk);
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t v[4];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
-                // dS: row = key r, chunk = this warpgroup's 64 queries
-                const uint32_t row_base = sdS + half * CHUNK_BYTES + r * 128;
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t addr = row_base + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * q]),
-                                 "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                                 : "memory");
+                        for (int e = 0; e < 4; ++e)
+                            v[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * mul,
+                                               __uint_as_float(o[8 * q + 2 * e + 1]) * mul);
+                        const uint32_t piece = static_cast<uint32_t>(half * 4 + q);
+                        const uint32_t addr = chunk_base + ((piece ^ static_cast<uint32_t>(r & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
+                                     "r"(v[2]), "r"(v[3])
+                                     : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    // both halves of every staged row are written
+                    ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
+                    if (!ok) break;
+                    if (half == 0 && lane == 0 && w.k0 + 32 * wq < p.m) {
+                        tma_store_3d(which == 0 ? &maps.dv : &maps.dk, sdS + wq * 32 * 128, 0, w.k0 + 32 * wq,
+                                     w.bh);
+                        bulk_commit_group();
+                        bulk_pending = true;
+                    }
+                    __syncwarp();
                 }
+                // (warpgroup 0 writes its dS rows of the next tile only after these
+                // stores have read them; warpgroup 1's dS chunk is not staging)
+                ++it;
             }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(L::B_PFULL));
-            if (t > 0) dq_out(t - 1);                 // waited for above (B_BDONE of t - 1)
         }
-        if (ok) {
+        if (ok && has_prev) {
             // the last tile's dQ
-            ok = mbar_wait(bar(L::B_BDONE), static_cast<uint32_t>(nt - 1) & 1u, abort_word, p.status,
+            ok = mbar_wait(bar(L::B_BDONE), static_cast<uint32_t>(gt - 1) & 1u, abort_word, p.status,
                            STATUS_SOFTMAX_WAIT, limit);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();
-                dq_out(nt - 1);
-            }
-        }
-
-        // ---------------------------------------- dV, then dK (x scale): TMEM -> bf16 staging -> TMA store
-        // The two warpgroups convert 32 columns each into one 64-column staging chunk
-        // (the dS area, free once every MMA is done); warpgroup 0 stores it.
-        if (ok) {
-            ok = mbar_wait(bar(L::B_DKVDONE), 0, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        bool st_pending = false;
-        if (ok) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t col = which == 0 ? L::DV_COL : L::DK_COL;
-                const float mul = which == 0 ? 1.f : p.scale;
-                if (st_pending && lane == 0) bulk_wait_group_read0();
-                __syncwarp();
-                ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
-                if (!ok) break;
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_base + col + 32 * half, o);
-                tmem_wait_ld();
-                const uint32_t chunk_base = sdS + r * 128;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t v[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        v[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * mul,
-                                           __uint_as_float(o[8 * q + 2 * e + 1]) * mul);
-                    const uint32_t piece = static_cast<uint32_t>(half * 4 + q);
-                    const uint32_t addr = chunk_base + ((piece ^ static_cast<uint32_t>(r & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
-                                 "r"(v[2]), "r"(v[3])
-                                 : "memory");
-                }
-                fence_proxy_async_smem();
-                ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
-                if (!ok) break;
-                if (half == 0 && lane == 0 && k0 + 32 * wq < p.m) {
-                    tma_store_3d(which == 0 ? &maps.dv : &maps.dk, sdS + wq * 32 * 128, 0, k0 + 32 * wq, bh);
-                    bulk_commit_group();
-                    st_pending = true;
-                }
-                __syncwarp();
+                dq_out();
             }
         }
         if (lane == 0) bulk_wait_group0();
@@ -973,7 +1127,13 @@ cudaError_t launch(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream)
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
-    const int64_t grid = static_cast<int64_t>(p.B) * p.H * p.num_kblocks;
+    int64_t grid = static_cast<int64_t>(p.B) * p.H * p.num_kblocks;
+    if (D == 64) {
+        // persistent: one CTA per SM over units of one or two key tiles
+        const int64_t units = static_cast<int64_t>(p.B) * p.H *
+                              (mask_is_causal(MASK) ? (p.num_kblocks + 1) / 2 : p.num_kblocks);
+        grid = units < p.num_sms ? units : p.num_sms;
+    }
     kern<<<static_cast<unsigned>(grid), L::NUM_THREADS, L::BYTES, stream>>>(maps, p);
     return cudaGetLastError();
 }
