@@ -16,6 +16,7 @@
 
 #include "../../include/attn.h"
 #include "attn_internal.h"
+#include "sm103a.cuh"
 
 namespace {
 
@@ -124,6 +125,7 @@ int make_map_f32(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* map, void* 
 
 __global__ void fill_no_keys_kernel(uint16_t* O, int64_t o_elems, float* LSE, int64_t rows)
 {
+    sm103a::griddep_wait();   // earlier kernels' reads and writes of O and LSE come first
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t i0 = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     for (int64_t i = i0; i < o_elems; i += stride) O[i] = 0;
@@ -200,9 +202,8 @@ int fill_no_keys(int64_t bh, int n, int d_v, void* O, float* LSE, cudaStream_t s
     const int64_t rows = bh * n;
     const int64_t elems = rows * d_v;
     const int64_t blocks = std::min<int64_t>((elems + 255) / 256, 152 * 8);
-    fill_no_keys_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<uint16_t*>(O), elems, LSE,
-                                                                       rows);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = attn::launch_pdl(fill_no_keys_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                                           static_cast<uint16_t*>(O), elems, LSE, rows);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("fill kernel launch", e);
 }
 
@@ -420,6 +421,7 @@ __global__ void bwd_prep_kernel(const uint16_t* __restrict__ O, const uint16_t* 
                                 float* __restrict__ lse2, float* __restrict__ dd, float4* __restrict__ dq_acc,
                                 int64_t dq_vec)
 {
+    sm103a::griddep_wait();   // O, dO and LSE of the earlier kernels are visible
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = tid; i < dq_vec; i += stride) dq_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -460,6 +462,7 @@ __global__ void bwd_prep_kernel(const uint16_t* __restrict__ O, const uint16_t* 
 // dQ = bf16(scale * accumulator), four elements per step.
 __global__ void bwd_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dQ, int64_t vec, float scale)
 {
+    sm103a::griddep_wait();   // the main kernel's reduce-adds into the accumulator are complete
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < vec; i += stride) {
         const float4 a = acc[i];
@@ -568,16 +571,14 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
 
     const int64_t dq_vec = bh * n * d_k / 4;
     const int64_t prep_threads = std::max<int64_t>(dq_vec, bh * ws.n_pad * (d_v / 8));
-    bwd_prep_kernel<<<static_cast<unsigned>(grid_for(prep_threads, 256)), 256, 0, st>>>(
-        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), LSE, bh, n, ws.n_pad, d_v, lse2, dd,
-        reinterpret_cast<float4*>(dq_acc), dq_vec);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = attn::launch_pdl(bwd_prep_kernel, dim3(static_cast<unsigned>(grid_for(prep_threads, 256))), dim3(256),
+                                     0, st, static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), LSE,
+                                     bh, n, ws.n_pad, d_v, lse2, dd, reinterpret_cast<float4*>(dq_acc), dq_vec);
     if (e != cudaSuccess) return fail_cuda("backward preparation kernel launch", e);
     e = d_k == 64 ? attn::launch_bwd_d64(mask_kind, maps, p, st) : attn::launch_bwd_d128(mask_kind, maps, p, st);
     if (e != cudaSuccess) return fail_cuda("backward kernel launch", e);
-    bwd_convert_kernel<<<static_cast<unsigned>(grid_for(dq_vec, 256)), 256, 0, st>>>(
-        reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dQ), dq_vec, p.scale);
-    e = cudaGetLastError();
+    e = attn::launch_pdl(bwd_convert_kernel, dim3(static_cast<unsigned>(grid_for(dq_vec, 256))), dim3(256), 0, st,
+                         reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dQ), dq_vec, p.scale);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("dQ conversion kernel launch", e);
 }
 

@@ -47,6 +47,28 @@ struct TensorMaps {
     CUtensorMap q, k, v, o;
 };
 
+// Launches `kern` with programmatic stream serialization: the grid may start
+// before the previous kernel in the stream has finished. Every kernel launched
+// this way executes griddepcontrol.wait before its first global-memory access,
+// so it still sees all the previous kernel's writes; what overlaps is the
+// launch itself and the set-up before that wait.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Kernel variants (see the kernel headers):
 //   KERNEL_DP   one query tile per CTA, P apart from S in tensor memory
 //   KERNEL_NT1  one query tile per CTA, P over S

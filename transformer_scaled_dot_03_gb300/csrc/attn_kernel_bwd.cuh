@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(Layout<D>::NUM_THREADS, 1)
 attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 {
     using L = Layout<D>;
+    griddep_wait();   // the preparation kernel's D, LSE rows and zeroed dQ accumulator are visible
     const int kb = static_cast<int>(blockIdx.x) % p.num_kblocks;
     const int bh = static_cast<int>(blockIdx.x) / p.num_kblocks;
     const int k0 = kb * BN;
@@ -709,6 +710,7 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    griddep_wait();   // nothing above reads global memory; the preparation kernel's outputs come after
 
     const uint32_t sK = sbase + L::K_OFF;
     const uint32_t sV = sbase + L::V_OFF;
@@ -1134,8 +1136,7 @@ cudaError_t launch(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream)
                               (mask_is_causal(MASK) ? (p.num_kblocks + 1) / 2 : p.num_kblocks);
         grid = units < p.num_sms ? units : p.num_sms;
     }
-    kern<<<static_cast<unsigned>(grid), L::NUM_THREADS, L::BYTES, stream>>>(maps, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(L::NUM_THREADS), L::BYTES, stream, maps, p);
 }
 
 }  // namespace bwd

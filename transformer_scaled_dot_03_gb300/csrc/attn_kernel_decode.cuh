@@ -79,6 +79,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                    const DecodeParams p)
 {
     using L = Layout<D>;
+    griddep_wait();   // the previous grid's writes (Q, the cache, the lengths) are visible
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -306,6 +307,7 @@ template <int D>
 __global__ void __launch_bounds__(D)
 attn_decode_combine_kernel(const DecodeParams p)
 {
+    griddep_wait();   // the partial results of the chunk kernel are visible
     const int64_t r = blockIdx.x;                 // (b*H + h) * n + i
     const int64_t bh = r / p.n, i = r % p.n;
     const int c = threadIdx.x;
@@ -340,11 +342,10 @@ cudaError_t launch(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeP
         configured[dev] = true;
     }
     const int64_t grid = static_cast<int64_t>(p.B) * p.H * p.num_splits;
-    kern<<<static_cast<unsigned>(grid), L::NUM_THREADS, L::BYTES, stream>>>(tmK, tmV, p);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(L::NUM_THREADS), L::BYTES, stream, tmK, tmV, p);
     if (e != cudaSuccess || p.num_splits == 1) return e;
-    attn_decode_combine_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(p.B) * p.H * p.n), D, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(attn_decode_combine_kernel<D>, dim3(static_cast<unsigned>(static_cast<int64_t>(p.B) * p.H * p.n)),
+                      dim3(D), 0, stream, p);
 }
 
 }  // namespace dec

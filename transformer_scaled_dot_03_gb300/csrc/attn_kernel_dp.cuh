@@ -227,6 +227,12 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Everything above touches no global memory: under a programmatic dependent
+    // launch it may run before the previous grid in the stream has finished,
+    // whose results (Q, K, V, the key lengths) are read only after this wait.
+    // (An explicit early trigger for the next grid measured slower than the
+    // implicit one at exit: its waiting CTAs shared the SMs with this grid's tail.)
+    griddep_wait();
 
     const uint32_t sQ = sbase + L::Q_OFF;
     const uint32_t sK = sbase + L::K_OFF;
@@ -618,8 +624,8 @@ cudaError_t launch(const TensorMaps& maps, const FwdParams& p, int num_sms, cuda
     }
     const int64_t slots = static_cast<int64_t>(num_sms) * L::CTAS_PER_SM;
     const int64_t grid = p.num_units < slots ? p.num_units : slots;
-    kern<<<static_cast<unsigned>(grid), L::NUM_THREADS, L::BYTES, stream>>>(maps.q, maps.k, maps.v, maps.o, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(L::NUM_THREADS), L::BYTES, stream, maps.q,
+                      maps.k, maps.v, maps.o, p);
 }
 
 }  // namespace dp

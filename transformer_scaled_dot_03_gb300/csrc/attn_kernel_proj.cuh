@@ -107,6 +107,7 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    griddep_wait();   // nothing above reads global memory; A, W and the bias come after
 
     if (warp == WARP_TMA) {
         if (lane == 0) {
@@ -300,8 +301,7 @@ cudaError_t launch(const ProjMaps& maps, const ProjParams& p, int num_sms, cudaS
     }
     const int tiles = p.tiles_m * p.tiles_n;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<static_cast<unsigned>(grid), NUM_THREADS, BYTES, stream>>>(maps, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NUM_THREADS), BYTES, stream, maps, p);
 }
 
 }  // namespace proj

@@ -428,6 +428,13 @@ __device__ __forceinline__ void regs_inc()
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their writes are visible (a no-op without that launch attribute).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 template <uint32_t N>
 __device__ __forceinline__ void regs_dec()
 {
