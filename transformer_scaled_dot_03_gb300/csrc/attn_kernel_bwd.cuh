@@ -842,6 +842,9 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     mma_ss_warp(tmem + L::DK_COL, dS_k + aoff, dQ_mn + boff, ID_KV,
                                 (cur.t > 0 || kk > 0) ? 1u : 0u);
                 }
+                // the last reads of this tile's Q and dO are issued: the producer may
+                // refill the slot (dQ = dS K below reads neither)
+                mma_commit_warp(bar(L::B_QEMPTY + s));
                 // the previous tile's dQ must have left its columns
                 if (gt > 0 && !wait(L::B_DQFREE, parity ^ 1u)) {
                     ok = false;
@@ -854,7 +857,6 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     mma_ss_warp(tmem + L::DQ_COL, dS_mn + off, dK_mn + off, ID_DQ, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_warp(bar(L::B_BDONE));
-                mma_commit_warp(bar(L::B_QEMPTY + s));
                 if (cur.t == cur.w.nt - 1) {
                     mma_commit_warp(bar(L::B_DKVDONE));
                     mma_commit_warp(bar(L::B_KVEMPTY + ks));
@@ -1014,8 +1016,10 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             pk[i] = pack_bf16x2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
-                        // an epilogue store may still be reading this warp's rows of the dS area
-                        wait_bulk_read();
+                        // at an item's first tile the previous item's dV / dK store may still
+                        // be reading this warp's rows of the dS area (the later bulk groups
+                        // of the item are dQ reduce-adds, which read the dQ staging only)
+                        if (t == 0) wait_bulk_read();
                         const uint32_t row_base = sdS + half * CHUNK_BYTES + r * 128;
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
@@ -1038,10 +1042,10 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 }
                 if (!ok) break;
 
-                // ---------------------------------------- this item's dV, then dK (x scale)
+                // ---------------------------------------- this item's dV and dK (x scale)
                 // Both are read out of tensor memory first (the next item's first dV, dK
-                // may then overwrite them); the two warpgroups convert 32 columns each into
-                // one 64-column staging chunk (in the dS area) and warpgroup 0 stores it.
+                // may then overwrite them), staged in the two chunks of the dS area and
+                // stored by one TMA store per warp.
                 ok = mbar_wait(bar(L::B_DKVDONE), static_cast<uint32_t>(it) & 1u, abort_word, p.status,
                                STATUS_SOFTMAX_WAIT, limit);
                 ok = __all_sync(0xffffffffu, ok);
@@ -1053,15 +1057,15 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(bar(L::B_DKVFREE));
-#pragma unroll 1
+                // dV (x 1) into dS chunk 0 and dK (x scale) into chunk 1, each warpgroup
+                // its 32 columns of every row; the dS area is free (the item's last dK
+                // and dQ, which read it, are complete) and no earlier bulk store is
+                // still reading it (waited for at this item's first tile)
+#pragma unroll
                 for (int which = 0; which < 2; ++which) {
                     const uint32_t* o = which == 0 ? ov : ok_;
                     const float mul = which == 0 ? 1.f : p.scale;
-                    wait_bulk_read();
-                    // both warpgroups' earlier stores have read the staging rows
-                    ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
-                    if (!ok) break;
-                    const uint32_t chunk_base = sdS + r * 128;
+                    const uint32_t chunk_base = sdS + which * CHUNK_BYTES + r * 128;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint32_t v[4];
@@ -1075,20 +1079,19 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                                      "r"(v[2]), "r"(v[3])
                                      : "memory");
                     }
-                    fence_proxy_async_smem();
-                    // both halves of every staged row are written
-                    ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
-                    if (!ok) break;
-                    if (half == 0 && lane == 0 && w.k0 + 32 * wq < p.m) {
-                        tma_store_3d(which == 0 ? &maps.dv : &maps.dk, sdS + wq * 32 * 128, 0, w.k0 + 32 * wq,
-                                     w.bh);
-                        bulk_commit_group();
-                        bulk_pending = true;
-                    }
-                    __syncwarp();
                 }
-                // (warpgroup 0 writes its dS rows of the next tile only after these
-                // stores have read them; warpgroup 1's dS chunk is not staging)
+                fence_proxy_async_smem();
+                // both halves of every staged row are written
+                ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
+                if (!ok) break;
+                // warpgroup 0 stores dV, warpgroup 1 dK: the rows of its lane quadrant
+                if (lane == 0 && w.k0 + 32 * wq < p.m) {
+                    tma_store_3d(half == 0 ? &maps.dv : &maps.dk, sdS + half * CHUNK_BYTES + wq * 32 * 128, 0,
+                                 w.k0 + 32 * wq, w.bh);
+                    bulk_commit_group();
+                    bulk_pending = true;
+                }
+                __syncwarp();
                 ++it;
             }
         }
