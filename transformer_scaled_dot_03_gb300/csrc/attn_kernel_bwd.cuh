@@ -561,8 +561,7 @@ struct LayoutPipe {
     static constexpr int B_DQFREE = B_BDONE + 1;    // dQ read out of tensor memory      (256 arrivals)
     static constexpr int B_DKVDONE = B_DQFREE + 1;  // an item's dV, dK complete         (commit)
     static constexpr int B_DKVFREE = B_DKVDONE + 1; // an item's dV, dK read out         (256 arrivals)
-    static constexpr int B_EPI = B_DKVFREE + 1;     // epilogue staging steps            (256 arrivals)
-    static constexpr int B_DRAIN = B_EPI + 1;
+    static constexpr int B_DRAIN = B_DKVFREE + 1;
     static constexpr int B_NEVER = B_DRAIN + 1;
     static constexpr int NBARS = B_NEVER + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
@@ -687,7 +686,6 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         mbar_init(bar(L::B_DQFREE), L::COMPUTE_THREADS);
         mbar_init(bar(L::B_DKVDONE), 1);
         mbar_init(bar(L::B_DKVFREE), L::COMPUTE_THREADS);
-        mbar_init(bar(L::B_EPI), L::COMPUTE_THREADS);
         mbar_init(bar(L::B_DRAIN), 1);
         mbar_init(bar(L::B_NEVER), 1);
         *abort_word = 0u;
@@ -845,6 +843,9 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 // the last reads of this tile's Q and dO are issued: the producer may
                 // refill the slot (dQ = dS K below reads neither)
                 mma_commit_warp(bar(L::B_QEMPTY + s));
+                // the item's dV and dK are final after its last tile's products above
+                // (its epilogue stages them outside the dS area, which dQ still reads)
+                if (cur.t == cur.w.nt - 1) mma_commit_warp(bar(L::B_DKVDONE));
                 // the previous tile's dQ must have left its columns
                 if (gt > 0 && !wait(L::B_DQFREE, parity ^ 1u)) {
                     ok = false;
@@ -858,7 +859,6 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 }
                 mma_commit_warp(bar(L::B_BDONE));
                 if (cur.t == cur.w.nt - 1) {
-                    mma_commit_warp(bar(L::B_DKVDONE));
                     mma_commit_warp(bar(L::B_KVEMPTY + ks));
                     ++it;
                 }
@@ -878,15 +878,9 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         const float sl2 = p.scale_log2;
         bool ok = true;
         bool bulk_pending = false;   // this warp has committed bulk groups (reduce-adds, stores)
-        int epi_phase = 0;
         int gt = 0, it = 0;
         int prev_q0 = 0, prev_bh = 0;
         bool has_prev = false;       // a tile whose dQ is still to be read out
-        auto rendezvous = [&](int b, uint32_t parity) -> bool {
-            mbar_arrive(bar(b));
-            const bool rr = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
-            return __all_sync(0xffffffffu, rr);
-        };
         auto wait_bulk_read = [&]() {
             if (bulk_pending && lane == 0) bulk_wait_group_read0();
             __syncwarp();
@@ -1016,10 +1010,6 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             pk[i] = pack_bf16x2(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1]));
-                        // at an item's first tile the previous item's dV / dK store may still
-                        // be reading this warp's rows of the dS area (the later bulk groups
-                        // of the item are dQ reduce-adds, which read the dQ staging only)
-                        if (t == 0) wait_bulk_read();
                         const uint32_t row_base = sdS + half * CHUNK_BYTES + r * 128;
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
@@ -1043,50 +1033,42 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 if (!ok) break;
 
                 // ---------------------------------------- this item's dV and dK (x scale)
-                // Both are read out of tensor memory first (the next item's first dV, dK
-                // may then overwrite them), staged in the two chunks of the dS area and
-                // stored by one TMA store per warp.
+                // Warpgroup 0 takes dV, warpgroup 1 dK: each warp reads its 32 rows, all
+                // 64 columns, out of tensor memory (the next item's first dV, dK may then
+                // overwrite them), stages them in its own dQ staging chunk (the last
+                // tile's dQ = dS K may still be reading the dS area) once its earlier
+                // reduce-adds have read it, and stores them with one TMA store.
                 ok = mbar_wait(bar(L::B_DKVDONE), static_cast<uint32_t>(it) & 1u, abort_word, p.status,
                                STATUS_SOFTMAX_WAIT, limit);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t ov[32], ok_[32];
-                tmem_ld32(tmem + lane_base + L::DV_COL + 32 * half, ov);
-                tmem_ld32(tmem + lane_base + L::DK_COL + 32 * half, ok_);
+                uint32_t o[64];
+                const uint32_t col = half == 0 ? L::DV_COL : L::DK_COL;
+                tmem_ld32(tmem + lane_base + col, o);
+                tmem_ld32(tmem + lane_base + col + 32, o + 32);
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(bar(L::B_DKVFREE));
-                // dV (x 1) into dS chunk 0 and dK (x scale) into chunk 1, each warpgroup
-                // its 32 columns of every row; the dS area is free (the item's last dK
-                // and dQ, which read it, are complete) and no earlier bulk store is
-                // still reading it (waited for at this item's first tile)
+                const float mul = half == 0 ? 1.f : p.scale;
+                wait_bulk_read();
+                const uint32_t chunk_base = sdQ + half * CHUNK_BYTES + r * 128;
 #pragma unroll
-                for (int which = 0; which < 2; ++which) {
-                    const uint32_t* o = which == 0 ? ov : ok_;
-                    const float mul = which == 0 ? 1.f : p.scale;
-                    const uint32_t chunk_base = sdS + which * CHUNK_BYTES + r * 128;
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t v[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t v[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            v[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * mul,
-                                               __uint_as_float(o[8 * q + 2 * e + 1]) * mul);
-                        const uint32_t piece = static_cast<uint32_t>(half * 4 + q);
-                        const uint32_t addr = chunk_base + ((piece ^ static_cast<uint32_t>(r & 7)) << 4);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
-                                     "r"(v[2]), "r"(v[3])
-                                     : "memory");
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        v[e] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * e]) * mul,
+                                           __uint_as_float(o[8 * q + 2 * e + 1]) * mul);
+                    const uint32_t addr = chunk_base + ((static_cast<uint32_t>(q) ^ static_cast<uint32_t>(r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
+                                 "r"(v[2]), "r"(v[3])
+                                 : "memory");
                 }
                 fence_proxy_async_smem();
-                // both halves of every staged row are written
-                ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
-                if (!ok) break;
-                // warpgroup 0 stores dV, warpgroup 1 dK: the rows of its lane quadrant
+                __syncwarp();
                 if (lane == 0 && w.k0 + 32 * wq < p.m) {
-                    tma_store_3d(half == 0 ? &maps.dv : &maps.dk, sdS + half * CHUNK_BYTES + wq * 32 * 128, 0,
+                    tma_store_3d(half == 0 ? &maps.dv : &maps.dk, sdQ + half * CHUNK_BYTES + wq * 32 * 128, 0,
                                  w.k0 + 32 * wq, w.bh);
                     bulk_commit_group();
                     bulk_pending = true;
