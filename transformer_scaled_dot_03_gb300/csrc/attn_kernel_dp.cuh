@@ -230,8 +230,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // Everything above touches no global memory: under a programmatic dependent
     // launch it may run before the previous grid in the stream has finished,
     // whose results (Q, K, V, the key lengths) are read only after this wait.
-    // (An explicit early trigger for the next grid measured slower than the
-    // implicit one at exit: its waiting CTAs shared the SMs with this grid's tail.)
+    // (Explicit triggers for the next grid, at a CTA's start or at its last
+    // unit, measured slower than the implicit one at this grid's completion.)
     griddep_wait();
 
     const uint32_t sQ = sbase + L::Q_OFF;
