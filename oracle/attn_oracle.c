@@ -61,8 +61,21 @@
  * Rows with no visible key contribute nothing (their o_i = 0 is constant).
  * Masked keys get dK_j = dV_j = 0.
  *
- * ORACLE_PLANT (compile-time, default 0, 1..11) plants one known mistake so that the
- * test suite can show that its pins catch it; the shipped build never sets it.
+ * Linear distance bias (oracle_attn_fwd_alibi, oracle_attn_rows_alibi).
+ * "第2章：完整的 Transformer 架构" §5.3 (ALiBi) subtracts from every scaled
+ * score a bias proportional to the distance between query and key, with a
+ * slope m_h of its own for each head:
+ *
+ *   s_j   = scale * q_i . k_j - m_h |i' - j|,   i' = i + (m - n)
+ *
+ * where i' is the query's position among the keys (the n queries are the last
+ * n of the m positions, as for the causal mask; i' = i when n = m). The masks,
+ * the softmax, the weighted sum and the LSE then proceed as above on these
+ * biased scores.
+ *
+ * ORACLE_PLANT (compile-time, default 0, 1..11, 14..16) plants one known mistake so
+ * that the test suite can show that its pins catch it; the shipped build never
+ * sets it.
  */
 #include <math.h>
 #include <pthread.h>
@@ -142,7 +155,7 @@ static int64_t clamp_len(const int32_t* key_lengths, int mask_kind, int64_t b, i
  */
 static void attn_row(const double* q, const double* Kh, const double* Vh, int64_t m,
                      int dk, int dv, int mask_kind, int64_t i, int64_t len, int64_t off,
-                     double scale, double* s, double* o, double* lse, double* w_out)
+                     double scale, double slope, double* s, double* o, double* lse, double* w_out)
 {
     /* 1. scaled scores of every key */
     for (int64_t j = 0; j < m; ++j) {
@@ -158,6 +171,14 @@ static void attn_row(const double* q, const double* Kh, const double* Vh, int64_
         s[j] = dot;                /* planted: scale dropped */
 #else
         s[j] = scale * dot;
+#endif
+        /* linear distance bias (zero slope: none) */
+#if ORACLE_PLANT == 14
+        s[j] += slope * fabs((double)(i + off - j));    /* planted: bias added */
+#elif ORACLE_PLANT == 15
+        s[j] -= slope * fabs((double)(i - j));          /* planted: query position not aligned */
+#else
+        s[j] -= slope * fabs((double)(i + off - j));
 #endif
     }
     /* 2. maximum over the visible keys */
@@ -205,11 +226,25 @@ typedef struct {
     int64_t B, H, n, m;
     int dk, dv, mask_kind;
     double scale;
+    const double* slopes;  /* per head [H], or NULL: no distance bias */
     double *O, *LSE, *W;
     const int64_t* rows;   /* NULL: all rows; else flat indices into [B*H*n] */
     int64_t nrows;
     int nthreads, tid;
 } job_t;
+
+/* Distance-bias slope of head h of batch entry b (0 without a bias). */
+static double head_slope(const job_t* jb, int64_t b, int64_t h)
+{
+    if (jb->slopes == NULL) return 0.0;
+#if ORACLE_PLANT == 16
+    (void)h;
+    return jb->slopes[b % jb->H];                 /* planted: slope indexed by batch entry */
+#else
+    (void)b;
+    return jb->slopes[h];
+#endif
+}
 
 static void* worker(void* arg)
 {
@@ -221,12 +256,13 @@ static void* worker(void* arg)
         for (int64_t bh = jb->tid; bh < jb->B * jb->H; bh += jb->nthreads) {
             int64_t b = bh / jb->H;
             int64_t len = clamp_len(jb->key_lengths, jb->mask_kind, b, jb->m);
+            double slope = head_slope(jb, b, bh % jb->H);
             const double* Kh = jb->K + bh * jb->m * jb->dk;
             const double* Vh = jb->V + bh * jb->m * jb->dv;
             for (int64_t i = 0; i < jb->n; ++i) {
                 int64_t r = bh * jb->n + i;
                 attn_row(jb->Q + r * jb->dk, Kh, Vh, jb->m, jb->dk, jb->dv, jb->mask_kind, i,
-                         len, jb->m - jb->n, jb->scale, s, jb->O + r * jb->dv, jb->LSE + r,
+                         len, jb->m - jb->n, jb->scale, slope, s, jb->O + r * jb->dv, jb->LSE + r,
                          jb->W ? jb->W + r * jb->m : NULL);
             }
         }
@@ -238,7 +274,8 @@ static void* worker(void* arg)
             int64_t len = clamp_len(jb->key_lengths, jb->mask_kind, b, jb->m);
             attn_row(jb->Q + r * jb->dk, jb->K + bh * jb->m * jb->dk,
                      jb->V + bh * jb->m * jb->dv, jb->m, jb->dk, jb->dv, jb->mask_kind, i, len,
-                     jb->m - jb->n, jb->scale, s, jb->O + k * jb->dv, jb->LSE + k, NULL);
+                     jb->m - jb->n, jb->scale, head_slope(jb, b, bh % jb->H), s,
+                     jb->O + k * jb->dv, jb->LSE + k, NULL);
         }
     }
     free(s);
@@ -288,7 +325,7 @@ static void head_bwd(const double* Qh, const double* Kh, const double* Vh, const
         double lse;
         for (int c = 0; c < dk; ++c) dq[c] = 0.0;
         /* forward of row i: on return w holds its weights (0 where masked) */
-        attn_row(q, Kh, Vh, m, dk, dv, mask_kind, i, len, m - n, scale, w, o, &lse, NULL);
+        attn_row(q, Kh, Vh, m, dk, dv, mask_kind, i, len, m - n, scale, 0.0, w, o, &lse, NULL);
         if (isinf(lse)) continue;          /* no visible key: o_i = 0 is constant */
         double D = 0.0;
         for (int64_t j = 0; j < m; ++j) {
@@ -375,7 +412,20 @@ int oracle_attn_fwd(const double* Q, const double* K, const double* V, int64_t B
 {
     if (bad_args(B, H, n, m, dk, dv, mask_kind)) return -1;
     if (uses_lengths(mask_kind) && key_lengths == NULL) return -1;
-    job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, O, LSE, W,
+    job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, NULL, O, LSE, W,
+                NULL, 0, nthreads, 0};
+    return run(jb);
+}
+
+/* Forward with the linear distance bias: slopes [H] holds m_h of every head. */
+int oracle_attn_fwd_alibi(const double* Q, const double* K, const double* V, int64_t B,
+                          int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind,
+                          const int32_t* key_lengths, const double* slopes, double scale,
+                          double* O, double* LSE, double* W, int nthreads)
+{
+    if (bad_args(B, H, n, m, dk, dv, mask_kind) || slopes == NULL) return -1;
+    if (uses_lengths(mask_kind) && key_lengths == NULL) return -1;
+    job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, slopes, O, LSE, W,
                 NULL, 0, nthreads, 0};
     return run(jb);
 }
@@ -391,7 +441,24 @@ int oracle_attn_rows(const double* Q, const double* K, const double* V, int64_t 
     if (uses_lengths(mask_kind) && key_lengths == NULL) return -1;
     for (int64_t k = 0; k < nrows; ++k)
         if (rows[k] < 0 || rows[k] >= B * H * n) return -1;
-    job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, O, LSE, NULL,
+    job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, NULL, O, LSE, NULL,
+                rows, nrows, nthreads, 0};
+    return run(jb);
+}
+
+/* Selected rows with the linear distance bias (slopes [H]). */
+int oracle_attn_rows_alibi(const double* Q, const double* K, const double* V, int64_t B,
+                           int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind,
+                           const int32_t* key_lengths, const double* slopes, double scale,
+                           const int64_t* rows, int64_t nrows, double* O, double* LSE,
+                           int nthreads)
+{
+    if (bad_args(B, H, n, m, dk, dv, mask_kind) || rows == NULL || nrows < 0 || slopes == NULL)
+        return -1;
+    if (uses_lengths(mask_kind) && key_lengths == NULL) return -1;
+    for (int64_t k = 0; k < nrows; ++k)
+        if (rows[k] < 0 || rows[k] >= B * H * n) return -1;
+    job_t jb = {Q, K, V, key_lengths, B, H, n, m, dk, dv, mask_kind, scale, slopes, O, LSE, NULL,
                 rows, nrows, nthreads, 0};
     return run(jb);
 }

@@ -69,6 +69,12 @@ def _load(plant: int = 0) -> ctypes.CDLL:
     lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p,
                                     ctypes.c_double, dp, dp, dp, ci]
     lib.oracle_attn_bwd.restype = ci
+    lib.oracle_attn_fwd_alibi.argtypes = [dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p, dp,
+                                          ctypes.c_double, dp, dp, dp, ci]
+    lib.oracle_attn_fwd_alibi.restype = ci
+    lib.oracle_attn_rows_alibi.argtypes = [dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p, dp,
+                                           ctypes.c_double, i64p, i64, dp, dp, ci]
+    lib.oracle_attn_rows_alibi.restype = ci
     _libs[plant] = lib
     return lib
 
@@ -114,43 +120,64 @@ def _shapes(Q, K, V):
     return B, H, n, m, dk, dv
 
 
-def attn_fwd(Q, K, V, mask="none", key_lengths=None, scale=None, *, threads=None,
+def _slopes(slopes, H):
+    if slopes is None:
+        return None
+    arr = _f64(slopes).reshape(-1)
+    if arr.size != H:
+        raise ValueError(f"slopes must hold one value per head ({H})")
+    return np.ascontiguousarray(arr)
+
+
+def attn_fwd(Q, K, V, mask="none", key_lengths=None, scale=None, *, slopes=None, threads=None,
              weights=False, plant=0):
     """Oracle forward. Returns (O [B,H,n,dv], LSE [B,H,n]) or, with weights=True,
-    (O, LSE, W [B,H,n,m]). ``scale`` defaults to 1/sqrt(d_k)."""
+    (O, LSE, W [B,H,n,m]). ``scale`` defaults to 1/sqrt(d_k). ``slopes`` [H] adds the
+    linear distance bias -slopes[h] * |i + m - n - j| to every scaled score."""
     Qd, Kd, Vd = _f64(Q), _f64(K), _f64(V)
     B, H, n, m, dk, dv = _shapes(Qd, Kd, Vd)
     sc = 1.0 / np.sqrt(dk) if scale is None else float(scale)
     lens = _lens(key_lengths, B)
+    sl = _slopes(slopes, H)
     O = np.zeros((B, H, n, dv))
     L = np.zeros((B, H, n))
     W = np.zeros((B, H, n, m)) if weights else None
-    rc = _load(plant).oracle_attn_fwd(
-        _ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
-        B, H, n, m, dk, dv, MASK_CODES[mask], _ptr(lens, ctypes.c_int32), sc,
-        _ptr(O, ctypes.c_double), _ptr(L, ctypes.c_double), _ptr(W, ctypes.c_double),
-        threads or min(default_threads(), 16))
+    lib = _load(plant)
+    common = (_ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
+              B, H, n, m, dk, dv, MASK_CODES[mask], _ptr(lens, ctypes.c_int32))
+    outs = (_ptr(O, ctypes.c_double), _ptr(L, ctypes.c_double), _ptr(W, ctypes.c_double),
+            threads or min(default_threads(), 16))
+    if sl is None:
+        rc = lib.oracle_attn_fwd(*common, sc, *outs)
+    else:
+        rc = lib.oracle_attn_fwd_alibi(*common, _ptr(sl, ctypes.c_double), sc, *outs)
     if rc != 0:
         raise RuntimeError(f"oracle_attn_fwd failed ({rc})")
     return (O, L, W) if weights else (O, L)
 
 
-def attn_rows(Q, K, V, rows, mask="none", key_lengths=None, scale=None, *, threads=None,
-              plant=0):
-    """Oracle outputs for selected flat rows (b*H*n + h*n + i): (O [k,dv], LSE [k])."""
+def attn_rows(Q, K, V, rows, mask="none", key_lengths=None, scale=None, *, slopes=None,
+              threads=None, plant=0):
+    """Oracle outputs for selected flat rows (b*H*n + h*n + i): (O [k,dv], LSE [k]).
+    ``slopes`` as for ``attn_fwd``."""
     Qd, Kd, Vd = _f64(Q), _f64(K), _f64(V)
     B, H, n, m, dk, dv = _shapes(Qd, Kd, Vd)
     sc = 1.0 / np.sqrt(dk) if scale is None else float(scale)
     lens = _lens(key_lengths, B)
+    sl = _slopes(slopes, H)
     r = np.ascontiguousarray(np.asarray(
         rows.cpu().numpy() if hasattr(rows, "cpu") else rows, dtype=np.int64).reshape(-1))
     O = np.zeros((r.size, dv))
     L = np.zeros((r.size,))
-    rc = _load(plant).oracle_attn_rows(
-        _ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
-        B, H, n, m, dk, dv, MASK_CODES[mask], _ptr(lens, ctypes.c_int32), sc,
-        _ptr(r, ctypes.c_int64), r.size, _ptr(O, ctypes.c_double), _ptr(L, ctypes.c_double),
-        threads or min(default_threads(), 16))
+    lib = _load(plant)
+    common = (_ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
+              B, H, n, m, dk, dv, MASK_CODES[mask], _ptr(lens, ctypes.c_int32))
+    tail = (_ptr(r, ctypes.c_int64), r.size, _ptr(O, ctypes.c_double), _ptr(L, ctypes.c_double),
+            threads or min(default_threads(), 16))
+    if sl is None:
+        rc = lib.oracle_attn_rows(*common, sc, *tail)
+    else:
+        rc = lib.oracle_attn_rows_alibi(*common, _ptr(sl, ctypes.c_double), sc, *tail)
     if rc != 0:
         raise RuntimeError(f"oracle_attn_rows failed ({rc})")
     return O, L
