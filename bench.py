@@ -158,6 +158,11 @@ def job_value(flops_per_rank, world, ms):
     return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
+def workload_slopes(w):
+    """Distance-bias slopes [H] of a workload with the linear bias, else None."""
+    return inputs.alibi_slopes(w.H) if w.alibi else None
+
+
 def make_workload(name):
     w = inputs.WORKLOADS[name]
     x = inputs.workload_inputs(w)
@@ -210,6 +215,9 @@ def run_ours(args):
     copies = max(2, math.ceil(2 * L2_BYTES / (in_bytes + out_bytes)))
     stream = torch.cuda.Stream(device=dev)
     lens_d = x.key_lengths.to(dev) if x.key_lengths is not None else None
+    slopes_d = workload_slopes(w).to(dev) if w.alibi else None
+    if w.alibi and (bwd or proj or decode):
+        raise SystemExit("the distance-bias workloads have a forward pass only")
     dO_h = inputs.make_grad_output(w.B, w.H, w.n, w.d_v, seed=100 + w.seed) if bwd else None
     sets = []
     if proj:
@@ -261,6 +269,9 @@ def run_ours(args):
         elif decode:
             Q, K, V, O, L = st
             attn.attn_decode(Q, K, V, w.mask, lens, x.scale, O=O, LSE=L, workspace=wsp, stream=on)
+        elif w.alibi:
+            Q, K, V, O, L = st
+            attn.attn_fwd_alibi(Q, K, V, slopes_d, w.mask, lens, x.scale, O=O, LSE=L, stream=on)
         else:
             Q, K, V, O, L = st
             attn.attn_fwd(Q, K, V, w.mask, lens, x.scale, O=O, LSE=L, stream=on)
@@ -421,6 +432,7 @@ def run_ours(args):
             "config": {"workload": w.name, "pass": args.pass_ if (bwd or proj) else ("decode" if decode else "fwd"),
                        "B": w.B, "H": w.H, "n": w.n, "m": w.m,
                        "d_k": w.d_k, "d_v": w.d_v, "mask": w.mask,
+                       "distance_bias": "alibi slopes 2^(-8h/H)" if w.alibi else None,
                        "key_lengths": [w.len_lo, w.len_hi] if w.mask in inputs.LENGTH_MASKS else None,
                        "global_batch": w.B * world, "parallelism": f"replicas{world}",
                        "l2": f"rotating {copies} input/output sets "
@@ -470,12 +482,14 @@ def cpu_baseline(w, x, seconds):
     # calibrate on a small sample, then size the sample to about `seconds`
     probe = inputs.sample_rows(w.B, w.H, w.n, min(total_rows, 64 * threads), seed=11)
     t0 = time.perf_counter()
-    oracle.attn_rows(x.Q, x.K, x.V, probe, w.mask, x.key_lengths, x.scale, threads=threads)
+    oracle.attn_rows(x.Q, x.K, x.V, probe, w.mask, x.key_lengths, x.scale, slopes=workload_slopes(w),
+                     threads=threads)
     dt = max(time.perf_counter() - t0, 1e-6)
     count = int(min(total_rows, max(probe.numel(), probe.numel() * seconds / dt)))
     rows = inputs.sample_rows(w.B, w.H, w.n, count, seed=12)
     t0 = time.perf_counter()
-    oracle.attn_rows(x.Q, x.K, x.V, rows, w.mask, x.key_lengths, x.scale, threads=threads)
+    oracle.attn_rows(x.Q, x.K, x.V, rows, w.mask, x.key_lengths, x.scale, slopes=workload_slopes(w),
+                         threads=threads)
     dt = time.perf_counter() - t0
     return {"value": round(per_row * rows.numel() / dt / 1e12, 6), "unit": UNIT, "cores": threads,
             "kind": "oracle", "seconds": round(dt, 2),
@@ -497,7 +511,8 @@ def run_reference(args):
     per_row = w.flops() / (w.B * w.H * w.n)
     probe = inputs.sample_rows(w.B, w.H, w.n, min(total_rows, 16 * threads), seed=21)
     t0 = time.perf_counter()
-    oracle.attn_rows(x.Q, x.K, x.V, probe, w.mask, x.key_lengths, x.scale, threads=threads)
+    oracle.attn_rows(x.Q, x.K, x.V, probe, w.mask, x.key_lengths, x.scale, slopes=workload_slopes(w),
+                     threads=threads)
     rate = probe.numel() / max(time.perf_counter() - t0, 1e-6)
     per_step = max(threads, int(rate * args.cpu_seconds / (args.steps + args.warmup)))
     per_step = min(per_step, total_rows)
@@ -505,7 +520,8 @@ def run_reference(args):
     for i in range(args.warmup + args.steps):
         rows = inputs.sample_rows(w.B, w.H, w.n, per_step, seed=1000 + i)
         t0 = time.perf_counter()
-        oracle.attn_rows(x.Q, x.K, x.V, rows, w.mask, x.key_lengths, x.scale, threads=threads)
+        oracle.attn_rows(x.Q, x.K, x.V, rows, w.mask, x.key_lengths, x.scale, slopes=workload_slopes(w),
+                         threads=threads)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             secs.append(dt)
@@ -533,7 +549,8 @@ def main():
     ap.add_argument("--steps", type=int, default=65536)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER + inputs.VARIANT_ORDER + inputs.DECODE_ORDER)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=inputs.WORKLOAD_ORDER + inputs.VARIANT_ORDER + inputs.DECODE_ORDER
+                    + inputs.ALIBI_ORDER)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "proj", "outproj"], default="fwd",
                     help="fwd: the forward (the headline); bwd: the backward of the same workload; "

@@ -97,6 +97,29 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
              float* LSE, void* stream);
 
 /*
+ * Attention forward with a linear distance bias ("第2章：完整的 Transformer 架构"
+ * §5.3, ALiBi): every scaled score gets a bias proportional to the distance
+ * between the query and the key, with a slope of its own for each head,
+ *
+ *     O = softmax(Q Kᵀ * scale - slope_h * D + M) V,   D_ij = |i + (m - n) - j|,
+ *
+ * i + (m - n) being the query's position among the keys (the n queries are the
+ * last n of the m positions, as for the causal mask; |i - j| when n = m). The
+ * masks combine with the bias as in attn_fwd, and LSE is the natural log of the
+ * masked sum of exp of the biased scaled scores.
+ *   slopes       device fp32 [H], caller-owned, 4-byte aligned: the slope of
+ *                every head in the units of the scaled scores (natural-log
+ *                domain). Any finite values; 0 is no bias.
+ *   other arguments as in attn_fwd; supported: d_k == d_v in {64, 128}.
+ * Returns ATTN_OK or a negative attn_status_t (INVALID_ARG when slopes is NULL,
+ * UNSUPPORTED when d_k != d_v); on error nothing is enqueued. Forward only:
+ * attn_bwd and attn_decode take no bias.
+ */
+int attn_fwd_alibi(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+                   int d_v, int mask_kind, const int32_t* key_lengths, const float* slopes, float scale,
+                   void* O, float* LSE, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. Returns ATTN_ERR_TIMEOUT if any kernel since the last call gave up on a
  * bounded wait (its outputs are then undefined), ATTN_ERR_CUDA if the

@@ -1,0 +1,145 @@
+"""GPU parity of the forward with the linear distance bias ("第2章：完整的 Transformer
+架构" §5.3, ALiBi) against the fp64 oracle, element by element, on seeded bf16
+inputs, through the C entry point attn_fwd_alibi.
+
+The bias makes the nearby keys dominate a row, so rows are sharper than without
+it and |O| approaches the largest |v_j|. The comparison therefore uses the
+format-aware bound of the forward's stress cases: |O - O_ref| <= 1e-2 + 2^-8
+(|O_ref| + A) elementwise, A = sum_j w_j |v_j| from the oracle run on |V| (2^-8 is
+the unit roundoff of bf16, which rounds both the weights P and the output), the
+mean error <= 1e-3 + 2^-8 mean(|O_ref| + A); LSE max-abs <= 1e-3. Outputs land in
+buffers with guard bands that must come back untouched.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from transformer_scaled_dot_03_gb300 import attn, build, inputs
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX = 1e-2, 1e-3, 1e-3
+BF16_U = 2.0 ** -8
+GUARD = 2048
+SENTINEL = -12345.0
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return attn.load()
+
+
+def run_gpu(x, slopes):
+    Q, K, V = x.Q.cuda(), x.K.cuda(), x.V.cuda()
+    lens = x.key_lengths.cuda() if x.key_lengths is not None else None
+    B, H, n, _ = Q.shape
+    dv = V.shape[3]
+    ob = torch.full((B * H * n * dv + 2 * GUARD,), SENTINEL, dtype=torch.bfloat16, device="cuda")
+    lb = torch.full((B * H * n + 2 * GUARD,), SENTINEL, dtype=torch.float32, device="cuda")
+    O = ob[GUARD:GUARD + B * H * n * dv].view(B, H, n, dv)
+    L = lb[GUARD:GUARD + B * H * n].view(B, H, n)
+    attn.attn_fwd_alibi(Q, K, V, slopes.cuda(), x.mask, lens, x.scale, O=O, LSE=L)
+    rc, detail = attn.device_status()
+    assert rc == attn.ATTN_OK, (rc, detail)
+    obc, lbc = ob.cpu(), lb.cpu()
+    for buf in (obc, lbc):
+        assert torch.all(buf[:GUARD] == SENTINEL) and torch.all(buf[-GUARD:] == SENTINEL), "guard band overwritten"
+    return O.float().cpu().numpy(), L.cpu().numpy()
+
+
+def compare(O, L, Or, Lr, A, label):
+    O = O.reshape(Or.shape)
+    L = L.reshape(Lr.shape)
+    assert np.all(np.isfinite(O)), f"{label}: non-finite O"
+    err = np.abs(O - Or)
+    excess = err - (O_MAX + BF16_U * (np.abs(Or) + A))
+    assert excess.max() <= 0, f"{label}: O error over the bound by {excess.max():.3e}"
+    assert err.mean() <= O_MEAN + BF16_U * (np.abs(Or) + A).mean(), f"{label}: O mean-abs {err.mean():.3e}"
+    empty = np.isneginf(Lr)
+    assert np.array_equal(np.isneginf(L), empty), f"{label}: -inf LSE pattern differs"
+    if (~empty).any():
+        assert np.all(np.isfinite(L[~empty])), f"{label}: non-finite LSE"
+        lerr = np.abs(L[~empty] - Lr[~empty]).max()
+        assert lerr <= LSE_MAX, f"{label}: LSE max-abs {lerr:.3e}"
+
+
+def check_full(x, slopes, label):
+    O, L = run_gpu(x, slopes)
+    Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale, slopes=slopes)
+    A, _ = oracle.attn_fwd(x.Q, x.K, x.V.abs(), x.mask, x.key_lengths, x.scale, slopes=slopes)
+    compare(O, L, Or, Lr, A, label)
+
+
+# ------------------------------------------------------------------ seeded workloads
+
+@pytest.mark.parametrize("name,count", [("alibi_decoder_causal", 4000), ("alibi_long_causal", 800)])
+def test_workload_sampled_rows(name, count):
+    """Full-size workload in the benchmark's launch configuration; the oracle computes
+    a seeded sample of rows (first and last included)."""
+    w = inputs.WORKLOADS[name]
+    x = inputs.workload_inputs(w)
+    slopes = inputs.alibi_slopes(w.H)
+    O, L = run_gpu(x, slopes)
+    rows = inputs.sample_rows(w.B, w.H, w.n, count, seed=100 + w.seed)
+    Or, Lr = oracle.attn_rows(x.Q, x.K, x.V, rows, x.mask, x.key_lengths, x.scale, slopes=slopes)
+    A, _ = oracle.attn_rows(x.Q, x.K, x.V.abs(), rows, x.mask, x.key_lengths, x.scale, slopes=slopes)
+    r = rows.numpy()
+    compare(O.reshape(-1, w.d_v)[r], L.reshape(-1)[r], Or, Lr, A, name)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+
+
+# ------------------------------------------------------------------ shapes, masks, slopes
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask,n,m", [("none", 200, 200), ("none", 100, 333), ("none", 257, 64),
+                                      ("causal", 300, 300), ("causal", 129, 400), ("causal", 300, 130),
+                                      ("key_padding", 150, 300), ("causal_key_padding", 260, 260)])
+def test_shapes_and_masks(d, mask, n, m):
+    lens = [m, max(1, m // 3), 1] if mask in inputs.LENGTH_MASKS else None
+    B = 3 if lens else 2
+    x = inputs.make_inputs(B, 4, n, m, d, d, mask, seed=5000 + n + m + d, key_lengths=lens)
+    check_full(x, inputs.alibi_slopes(4), f"{mask} n={n} m={m} d={d}")
+
+
+def test_slope_range():
+    """Zero, tiny, steep and negative slopes in one call (one per head)."""
+    x = inputs.make_inputs(2, 5, 300, 300, 64, 64, "none", seed=5100)
+    slopes = torch.tensor([0.0, 1e-4, 2.0, -0.03, 0.5], dtype=torch.float32)
+    check_full(x, slopes, "slope range")
+
+
+def test_zero_slopes_match_attn_fwd():
+    x = inputs.make_inputs(2, 3, 200, 200, 128, 128, "causal", seed=5200)
+    O, L = run_gpu(x, torch.zeros(3))
+    O0, L0 = attn.attn_fwd(x.Q.cuda(), x.K.cuda(), x.V.cuda(), "causal", None, x.scale)
+    assert np.abs(O - O0.float().cpu().numpy()).max() <= 1e-2
+    assert np.abs(L - L0.cpu().numpy()).max() <= 1e-4
+
+
+def test_rejected_arguments():
+    lib = attn.load()
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16, device="cuda")
+    q2 = torch.zeros(1, 2, 4, 128, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros_like(q2)
+    sl = torch.zeros(2, device="cuda")
+    vp = ctypes.c_void_p
+    stream = vp(torch.cuda.current_stream().cuda_stream)
+    # no slopes
+    rc = lib.attn_fwd_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), 1, 2, 4, 4, 64, 64, 0, None, None,
+                            ctypes.c_float(-1.0), vp(o.data_ptr()), None, stream)
+    assert rc == attn.ATTN_ERR_INVALID_ARG
+    # d_k != d_v
+    rc = lib.attn_fwd_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q2.data_ptr()), 1, 2, 4, 4, 64, 128, 0, None,
+                            vp(sl.data_ptr()), ctypes.c_float(-1.0), vp(o.data_ptr()), None, stream)
+    assert rc == attn.ATTN_ERR_UNSUPPORTED
+    # misaligned slopes
+    rc = lib.attn_fwd_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), 1, 2, 4, 4, 64, 64, 0, None,
+                            vp(sl.data_ptr() + 2), ctypes.c_float(-1.0), vp(o.data_ptr()), None, stream)
+    assert rc == attn.ATTN_ERR_MISALIGNED

@@ -32,7 +32,7 @@ MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PAD
               _inputs.MASK_CAUSAL_KEY_PADDING: 3}
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_fwd", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
+EXPORTS = ("attn_fwd", "attn_fwd_alibi", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
            "attn_last_error", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
            "attn_decode_workspace_size", "attn_proj_heads", "attn_merge_proj")
 
@@ -59,6 +59,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         lib.attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp]
         lib.attn_fwd.restype = i32
+        lib.attn_fwd_alibi.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp]
+        lib.attn_fwd_alibi.restype = i32
         lib.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
         lib.attn_get_device_status.restype = i32
         lib.attn_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
@@ -144,6 +146,43 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "non
                       _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd", last_error() if rc == ATTN_ERR_CUDA else "")
+    return O, LSE
+
+
+def attn_fwd_alibi(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, slopes: torch.Tensor,
+                   mask: str = "none", key_lengths: torch.Tensor | None = None, scale: float | None = None,
+                   O: torch.Tensor | None = None, LSE: torch.Tensor | None = None,
+                   want_lse: bool = True, stream=None):
+    """Attention forward with the linear distance bias -slopes[h] * |i + m - n - j| added
+    to every scaled score (ALiBi). ``slopes`` is a contiguous fp32 CUDA tensor [H];
+    everything else as in ``attn_fwd`` (d_k == d_v in {64, 128})."""
+    if mask not in MASK_CODES:
+        raise ValueError(f"unknown mask {mask!r}")
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor")
+    B, H, n, d_k = Q.shape
+    m = K.shape[2]
+    d_v = V.shape[3]
+    if tuple(K.shape) != (B, H, m, d_k) or tuple(V.shape[:3]) != (B, H, m):
+        raise ValueError("inconsistent Q/K/V shapes")
+    if slopes.dtype != torch.float32 or not slopes.is_cuda or slopes.numel() != H or not slopes.is_contiguous():
+        raise ValueError("slopes must be a contiguous fp32 CUDA tensor with one value per head")
+    uses_lengths = mask in _inputs.LENGTH_MASKS
+    if uses_lengths:
+        if key_lengths is None or key_lengths.dtype != torch.int32 or not key_lengths.is_cuda \
+                or key_lengths.numel() != B or not key_lengths.is_contiguous():
+            raise ValueError(f"{mask} needs key_lengths: contiguous int32 CUDA [B]")
+    if O is None:
+        O = torch.empty((B, H, n, d_v), dtype=torch.bfloat16, device=Q.device)
+    if LSE is None and want_lse:
+        LSE = torch.empty((B, H, n), dtype=torch.float32, device=Q.device)
+    sc = -1.0 if scale is None else float(scale)
+    rc = load().attn_fwd_alibi(_ptr(Q), _ptr(K), _ptr(V), int(B), int(H), int(n), int(m), int(d_k), int(d_v),
+                               MASK_CODES[mask], _ptr(key_lengths) if uses_lengths else None, _ptr(slopes),
+                               ctypes.c_float(sc), _ptr(O), _ptr(LSE), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_alibi", last_error() if rc == ATTN_ERR_CUDA else "")
     return O, LSE
 
 

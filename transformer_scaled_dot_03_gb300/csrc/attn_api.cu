@@ -208,13 +208,14 @@ int fill_no_keys(int64_t bh, int n, int d_v, void* O, float* LSE, cudaStream_t s
 }
 
 // Tensor maps, parameters and the launch of the attention kernel (m >= 1),
-// with `status` as the kernel's device status word.
+// with `status` as the kernel's device status word; `slopes` (device fp32 [H])
+// selects the kernel with the linear distance bias, null the plain one.
 int launch_attention(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
                      int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
-                     uint32_t* status, cudaStream_t st)
+                     uint32_t* status, cudaStream_t st, const float* slopes = nullptr)
 {
     const int64_t bh = static_cast<int64_t>(B) * H;
-    const int variant = kernel_variant(d_k, d_v, mask_kind, n, m);
+    const int variant = slopes != nullptr ? static_cast<int>(attn::KERNEL_DP) : kernel_variant(d_k, d_v, mask_kind, n, m);
     const int64_t rows_per_cta = attn::kernel_rows_per_cta(variant);
     const int64_t num_qblocks = (static_cast<int64_t>(n) + rows_per_cta - 1) / rows_per_cta;
 
@@ -242,6 +243,7 @@ int launch_attention(const void* Q, const void* K, const void* V, int B, int H, 
     p.key_lengths = attn::mask_has_lengths(mask_kind) ? key_lengths : nullptr;
     p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
     p.LSE = LSE;
+    p.slopes = slopes;
     p.status = status;
     p.watchdog_ns = g_watchdog_ns;
     p.debug_flags = g_debug_flags;
@@ -250,7 +252,9 @@ int launch_attention(const void* Q, const void* K, const void* V, int B, int H, 
     if ((rc = sm_count(&num_sms)) != ATTN_OK) return rc;
     const int64_t ctas = bh * num_qblocks;
     cudaError_t e;
-    if (d_k != d_v)
+    if (slopes != nullptr)
+        e = attn::launch_fwd_alibi(d_k, mask_kind, maps, p, num_sms, st);
+    else if (d_k != d_v)
         e = attn::launch_fwd_dmix(d_k, d_v, mask_kind, maps, p, num_sms, st);
     else if (d_k == 64)
         e = attn::launch_fwd_d64(mask_kind, variant, maps, p, ctas, num_sms, st);
@@ -274,6 +278,23 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
     uint32_t* status = nullptr;
     if ((rc = status_word(&status)) != ATTN_OK) return rc;
     return launch_attention(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, scale, O, LSE, status, st);
+}
+
+int attn_fwd_alibi(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+                   int d_v, int mask_kind, const int32_t* key_lengths, const float* slopes, float scale,
+                   void* O, float* LSE, void* stream)
+{
+    int rc = validate(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, O, LSE);
+    if (rc != ATTN_OK || B == 0 || H == 0 || n == 0) return rc;
+    if (d_k != d_v) return ATTN_ERR_UNSUPPORTED;
+    if (slopes == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(slopes, 4)) return ATTN_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (m == 0) return fill_no_keys(static_cast<int64_t>(B) * H, n, d_v, O, LSE, st);
+    uint32_t* status = nullptr;
+    if ((rc = status_word(&status)) != ATTN_OK) return rc;
+    return launch_attention(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, scale, O, LSE, status, st,
+                            slopes);
 }
 
 int attn_get_device_status(void* stream, uint32_t* detail)

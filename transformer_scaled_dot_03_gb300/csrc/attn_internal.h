@@ -38,6 +38,7 @@ struct FwdParams {
     const int32_t* key_lengths;   // device int32 [B] (key-padding masks only)
     float scale_log2;             // scale * log2(e)
     float* LSE;                   // fp32 [B,H,n] or null
+    const float* slopes;          // fp32 [H]: distance-bias slope per head (bias kernels only)
     uint32_t* status;             // device status word
     uint64_t watchdog_ns;         // wall-clock limit of one bounded wait
     uint32_t debug_flags;
@@ -154,5 +155,8 @@ cudaError_t launch_fwd_d128(int mask, int variant, const TensorMaps& maps, const
 // d_k != d_v (64 and 128 either way round), persistent kernel only.
 cudaError_t launch_fwd_dmix(int d_k, int d_v, int mask, const TensorMaps& maps, const FwdParams& p,
                             int num_sms, cudaStream_t stream);
+// Forward with the linear distance bias (p.slopes), d_k = d_v = d in {64, 128}.
+cudaError_t launch_fwd_alibi(int d, int mask, const TensorMaps& maps, const FwdParams& p, int num_sms,
+                             cudaStream_t stream);
 
 }  // namespace attn

@@ -29,6 +29,13 @@
 //   otherwise     : 512 columns, up to 224 KB shared memory -> one CTA per SM
 // O leaves through a shared-memory staging tile and per-warp TMA stores that
 // are only waited for before the staging tile is reused.
+//
+// BIAS adds the linear distance bias of "第2章：完整的 Transformer 架构" §5.3
+// (ALiBi): every scaled score gets -m_h |i' - j|, i' = i + (m - n) the query's
+// position among the keys and m_h the slope of the head. The softmax warps form
+// x = s * scale*log2e + bias first (a ramp in the column when the whole tile lies
+// on one side of a warp's diagonal, the distance itself on the tiles that
+// straddle it) and take the row maximum and the exponentials of x.
 #pragma once
 
 #include <cstdint>
@@ -48,6 +55,7 @@ constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int CHUNK_BYTES = BM * 64 * 2;
 constexpr float LN2 = 0.693147180559945309f;
+constexpr float LOG2E = 1.44269504088896341f;
 // The reference maximum of a row is only raised when a new score exceeds it by
 // more than 2^8; until then exp2(x - m_ref) <= 2^8, which bf16 P and the fp32
 // sums hold as well as values <= 1, and O needs no rescaling.
@@ -170,7 +178,7 @@ __device__ __forceinline__ void advance(TilePos& t, int u_step, const FwdParams&
     }
 }
 
-template <int DK, int DV, int MASK>
+template <int DK, int DV, int MASK, bool BIAS>
 __global__ void __launch_bounds__(Layout<DK, DV>::NUM_THREADS, Layout<DK, DV>::CTAS_PER_SM)
 attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -428,7 +436,9 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (TilePos t = first_tile; ok && t.u < p.num_units; advance<MASK>(t, u_step, p)) {
             const Unit w = tile_of<MASK>(t.u, t.ti, p);
             const int qrow = w.q0 + r;
-            const int qlim = qrow + p.causal_off;   // last key this row sees under the causal mask
+            const int qlim = qrow + p.causal_off;   // the row's key position: last key it sees under the causal mask
+            // distance-bias slope of the head, log2 domain
+            const float sb = BIAS ? __ldg(p.slopes + w.bh % p.H) * LOG2E : 0.f;
             float m_ref = -INFINITY;
             float l_run = 0.f;
             if (L::Q_IN_TMEM && w.nkv > 0 && !(q_done.u == t.u && q_done.ti == t.ti)) {
@@ -466,6 +476,36 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     for (int c = 0; c < BN; ++c)
                         if (c >= c_hi) s[c] = -INFINITY;
                 }
+                const uint64_t sl22 = f2_pack(sl2, sl2);
+                if (BIAS) {
+                    // x_c = s_c * scale*log2e - sb |d0 - c|, d0 the row's key position
+                    // relative to the tile's first key
+                    const float d0 = static_cast<float>(qlim - key0);
+                    // Under a causal mask every column past d0 is already -inf, so the
+                    // left-side ramp serves the diagonal tile too.
+                    const bool left =
+                        mask_is_causal(MASK) || __all_sync(0xffffffffu, d0 >= static_cast<float>(BN - 1));
+                    const bool right = !left && __all_sync(0xffffffffu, d0 <= 0.f);
+                    if (left || right) {
+                        // the tile lies on one side of every row's diagonal: the bias is
+                        // sg (c - d0), stepped along four interleaved column ramps
+                        const float sg = left ? sb : -sb;
+                        uint64_t r2[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            r2[k] = f2_pack(sg * (static_cast<float>(2 * k) - d0), sg * (static_cast<float>(2 * k + 1) - d0));
+                        const uint64_t st2 = f2_pack(8.f * sg, 8.f * sg);
+#pragma unroll
+                        for (int c = 0; c < BN / 2; ++c) {
+                            const uint64_t x2 = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl22, r2[c % 4]);
+                            r2[c % 4] = f2_add(r2[c % 4], st2);
+                            f2_unpack(x2, s[2 * c], s[2 * c + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < BN; ++c) s[c] = fmaf(-sb, fabsf(d0 - static_cast<float>(c)), s[c] * sl2);
+                    }
+                }
                 // row maximum: eight independent chains of three-input max
                 float mx[8];
 #pragma unroll
@@ -474,21 +514,22 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int c = 16; c < BN; c += 16)
 #pragma unroll
                     for (int k = 0; k < 8; ++k) mx[k] = max3f(mx[k], s[c + 2 * k], s[c + 2 * k + 1]);
-                const float tile_max =
-                    max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+                // (with the bias the scores are already in the log2 domain)
+                const float tile_max = max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]),
+                                             fmaxf(mx[6], mx[7])) * (BIAS ? 1.f : sl2);
                 const bool raise = tile_max > m_ref + RESCALE_LOG2;
                 const float m_new = raise ? tile_max : m_ref;
                 const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
                 const float alpha = raise ? ex2_approx(m_ref - m_use) : 1.f;
 
                 // p = exp2(s * scale*log2e - m) on score pairs (packed fp32 arithmetic)
-                const uint64_t sl22 = f2_pack(sl2, sl2);
+                const uint64_t mul2 = BIAS ? f2_pack(1.f, 1.f) : sl22;
                 const uint64_t nm2 = f2_pack(-m_use, -m_use);
                 uint32_t pk[BN / 2];
                 uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int c = 0; c < BN / 2; ++c) {
-                    const uint64_t x2 = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl22, nm2);
+                    const uint64_t x2 = f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), mul2, nm2);
                     float a, b;
                     f2_unpack(x2, a, b);
                     const uint64_t p2 = f2_pack(ex2_approx(a), ex2_approx(b));
@@ -607,11 +648,11 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
 }
 
-template <int DK, int DV, int MASK>
+template <int DK, int DV, int MASK, bool BIAS = false>
 cudaError_t launch(const TensorMaps& maps, const FwdParams& p, int num_sms, cudaStream_t stream)
 {
     using L = Layout<DK, DV>;
-    auto kern = attn_fwd_dp_kernel<DK, DV, MASK>;
+    auto kern = attn_fwd_dp_kernel<DK, DV, MASK, BIAS>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -62,6 +62,7 @@ class Workload:
     len_hi: int = 0
     d_model: int = 0                # projection recipe only
     path: str = "fwd"               # "fwd": attn_fwd; "decode": the few-row attn_decode
+    alibi: bool = False             # linear distance bias with the slopes of alibi_slopes(H)
 
     def flops(self) -> float:
         """Nominal forward FLOPs: 2*d_k (scores) + 2*d_v (weighted sum) per visible
@@ -127,6 +128,22 @@ WORKLOADS.update({
                                     path="decode"),
 })
 DECODE_ORDER = ["decode_kv_cache", "decode_long_context"]
+
+# The linear distance bias ("第2章：完整的 Transformer 架构" §5.3) on the big-decoder
+# and the long-context causal self-attention.
+WORKLOADS.update({
+    "alibi_decoder_causal": Workload("alibi_decoder_causal", 16, 16, 1024, 1024, 64, 64, MASK_CAUSAL,
+                                     seed=10, alibi=True),
+    "alibi_long_causal": Workload("alibi_long_causal", 4, 16, 8192, 8192, 128, 128, MASK_CAUSAL,
+                                  seed=11, value_scale=0.5, alibi=True),
+})
+ALIBI_ORDER = ["alibi_decoder_causal", "alibi_long_causal"]
+
+
+def alibi_slopes(H: int) -> torch.Tensor:
+    """Distance-bias slopes, one per head: the geometric sequence 2^(-8 h / H),
+    h = 1..H, of the linear-bias method's paper. fp32 CPU tensor [H]."""
+    return torch.tensor([2.0 ** (-8.0 * h / H) for h in range(1, H + 1)], dtype=torch.float32)
 
 
 @dataclasses.dataclass
