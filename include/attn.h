@@ -112,8 +112,8 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
  *                domain). Any finite values; 0 is no bias.
  *   other arguments as in attn_fwd; supported: d_k == d_v in {64, 128}.
  * Returns ATTN_OK or a negative attn_status_t (INVALID_ARG when slopes is NULL,
- * UNSUPPORTED when d_k != d_v); on error nothing is enqueued. Forward only:
- * attn_bwd and attn_decode take no bias.
+ * UNSUPPORTED when d_k != d_v); on error nothing is enqueued. Its decoding
+ * form is attn_decode_alibi; attn_bwd takes no bias.
  */
 int attn_fwd_alibi(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
                    int d_v, int mask_kind, const int32_t* key_lengths, const float* slopes, float scale,
@@ -231,6 +231,18 @@ size_t attn_decode_workspace_size(int B, int H, int n, int m, int d_k, int d_v);
 int attn_decode(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
                 int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_decode with the linear distance bias of attn_fwd_alibi ("第2章：完整的
+ * Transformer 架构" §5.3, ALiBi): score of row i and key j minus
+ * slopes[h] * |i + (m - n) - j|, i + (m - n) being the new token's position in
+ * the cache. `slopes` is a device fp32 [H] array (4-byte aligned, caller-owned);
+ * everything else as in attn_decode, including the workspace (the same size).
+ * ATTN_ERR_INVALID_ARG when slopes is NULL.
+ */
+int attn_decode_alibi(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+                      int d_v, int mask_kind, const int32_t* key_lengths, const float* slopes, float scale,
+                      void* O, float* LSE, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The projections around the attention ("从 RNN 到 Transformer（二）" §4.6,

@@ -1,6 +1,7 @@
 """GPU parity of the forward with the linear distance bias ("第2章：完整的 Transformer
 架构" §5.3, ALiBi) against the fp64 oracle, element by element, on seeded bf16
-inputs, through the C entry point attn_fwd_alibi.
+inputs, through the C entry points attn_fwd_alibi and attn_decode_alibi (the
+few-row decoding form).
 
 The bias makes the nearby keys dominate a row, so rows are sharper than without
 it and |O| approaches the largest |v_j|. The comparison therefore uses the
@@ -143,3 +144,50 @@ def test_rejected_arguments():
     rc = lib.attn_fwd_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), 1, 2, 4, 4, 64, 64, 0, None,
                             vp(sl.data_ptr() + 2), ctypes.c_float(-1.0), vp(o.data_ptr()), None, stream)
     assert rc == attn.ATTN_ERR_MISALIGNED
+
+
+# ------------------------------------------------------------------ decoding (attn_decode_alibi)
+
+def run_decode(x, slopes):
+    Q, K, V = x.Q.cuda(), x.K.cuda(), x.V.cuda()
+    lens = x.key_lengths.cuda() if x.key_lengths is not None else None
+    O, L = attn.attn_decode(Q, K, V, x.mask, lens, x.scale, slopes=slopes.cuda())
+    rc, detail = attn.device_status()
+    assert rc == attn.ATTN_OK, (rc, detail)
+    return O.float().cpu().numpy(), L.cpu().numpy()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask,n,m", [("none", 1, 4097), ("none", 8, 129), ("causal", 4, 1000),
+                                      ("causal", 8, 5), ("key_padding", 1, 3000),
+                                      ("causal_key_padding", 3, 2100)])
+def test_decode(d, mask, n, m):
+    """Few query rows against a long key sequence (one and several key chunks per head)."""
+    lens = [m, m // 2 + 1, 1] if mask in inputs.LENGTH_MASKS else None
+    B = 3 if lens else 2
+    x = inputs.make_inputs(B, 4, n, m, d, d, mask, seed=5300 + n + m + d, key_lengths=lens)
+    slopes = inputs.alibi_slopes(4)
+    O, L = run_decode(x, slopes)
+    Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale, slopes=slopes)
+    A, _ = oracle.attn_fwd(x.Q, x.K, x.V.abs(), x.mask, x.key_lengths, x.scale, slopes=slopes)
+    compare(O, L, Or, Lr, A, f"decode {mask} n={n} m={m} d={d}")
+
+
+def test_decode_matches_forward():
+    """The decoding form gives the forward's result for the same rows."""
+    x = inputs.make_inputs(2, 8, 4, 2000, 128, 128, "causal", seed=5400)
+    slopes = inputs.alibi_slopes(8)
+    O, L = run_decode(x, slopes)
+    Of, Lf = run_gpu(x, slopes)
+    assert np.abs(O - Of).max() <= 2e-2
+    assert np.abs(L - Lf).max() <= 1e-3
+
+
+def test_decode_rejects_null_slopes():
+    lib = attn.load()
+    q = torch.zeros(1, 1, 1, 64, dtype=torch.bfloat16, device="cuda")
+    vp = ctypes.c_void_p
+    rc = lib.attn_decode_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), 1, 1, 1, 1, 64, 64, 0, None,
+                               None, ctypes.c_float(-1.0), vp(q.data_ptr()), None, None, ctypes.c_size_t(0),
+                               vp(torch.cuda.current_stream().cuda_stream))
+    assert rc == attn.ATTN_ERR_INVALID_ARG

@@ -32,7 +32,7 @@ MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PAD
               _inputs.MASK_CAUSAL_KEY_PADDING: 3}
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_fwd", "attn_fwd_alibi", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
+EXPORTS = ("attn_fwd", "attn_fwd_alibi", "attn_decode_alibi", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
            "attn_last_error", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
            "attn_decode_workspace_size", "attn_proj_heads", "attn_merge_proj")
 
@@ -75,6 +75,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp,
                                     ctypes.c_size_t, vp]
         lib.attn_decode.restype = i32
+        lib.attn_decode_alibi.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp,
+                                          ctypes.c_size_t, vp]
+        lib.attn_decode_alibi.restype = i32
         lib.attn_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_decode_workspace_size.restype = ctypes.c_size_t
         lib.attn_proj_heads.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
@@ -260,11 +263,12 @@ def attn_decode_raw(Q_ptr, K_ptr, V_ptr, B, H, n, m, d_k, d_v, mask_kind, key_le
 def attn_decode(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "none",
                 key_lengths: torch.Tensor | None = None, scale: float | None = None,
                 O: torch.Tensor | None = None, LSE: torch.Tensor | None = None, want_lse: bool = True,
-                workspace: torch.Tensor | None = None, stream=None):
+                workspace: torch.Tensor | None = None, stream=None, slopes: torch.Tensor | None = None):
     """Few-row attention forward (n <= 8 query rows per head against m keys, e.g. one
     decoding step against a key/value cache): same arguments and results as
     ``attn_fwd``. ``workspace`` (uint8 CUDA tensor of at least ``decode_workspace_size``
-    bytes) is allocated here when omitted and needed."""
+    bytes) is allocated here when omitted and needed. ``slopes`` (contiguous fp32 CUDA
+    [H]) adds the linear distance bias of ``attn_fwd_alibi`` (attn_decode_alibi)."""
     if mask not in MASK_CODES:
         raise ValueError(f"unknown mask {mask!r}")
     for name, t in (("Q", Q), ("K", K), ("V", V)):
@@ -290,10 +294,18 @@ def attn_decode(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "
     if workspace is not None and (workspace.numel() < ws_bytes or workspace.dtype != torch.uint8):
         raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {ws_bytes} bytes")
     sc = -1.0 if scale is None else float(scale)
-    rc = attn_decode_raw(_ptr(Q), _ptr(K), _ptr(V), B, H, n, m, d_k, d_v, MASK_CODES[mask],
-                         _ptr(key_lengths) if uses_lengths else None, sc, _ptr(O), _ptr(LSE),
-                         _ptr(workspace), 0 if workspace is None else workspace.numel(),
-                         _stream_handle(stream))
+    lens_p = _ptr(key_lengths) if uses_lengths else None
+    ws_n = 0 if workspace is None else workspace.numel()
+    if slopes is None:
+        rc = attn_decode_raw(_ptr(Q), _ptr(K), _ptr(V), B, H, n, m, d_k, d_v, MASK_CODES[mask], lens_p, sc,
+                             _ptr(O), _ptr(LSE), _ptr(workspace), ws_n, _stream_handle(stream))
+    else:
+        if slopes.dtype != torch.float32 or not slopes.is_cuda or slopes.numel() != H or not slopes.is_contiguous():
+            raise ValueError("slopes must be a contiguous fp32 CUDA tensor with one value per head")
+        rc = load().attn_decode_alibi(_ptr(Q), _ptr(K), _ptr(V), int(B), int(H), int(n), int(m), int(d_k),
+                                      int(d_v), MASK_CODES[mask], lens_p, _ptr(slopes), ctypes.c_float(sc), _ptr(O),
+                                      _ptr(LSE), _ptr(workspace), ctypes.c_size_t(ws_n),
+                                      ctypes.c_void_p(_stream_handle(stream)))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode", last_error() if rc == ATTN_ERR_CUDA else "")
     return O, LSE

@@ -659,9 +659,12 @@ extern "C" size_t attn_decode_workspace_size(int B, int H, int n, int m, int d_k
     return round_up(rows * d_k * 4, kWsAlign) + round_up(rows * 2 * 4, kWsAlign);
 }
 
-extern "C" int attn_decode(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
-                           int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
-                           void* workspace, size_t workspace_bytes, void* stream)
+namespace {
+
+// The few-row forward; `slopes` (device fp32 [H]) adds the linear distance bias, null none.
+int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k, int d_v,
+                int mask_kind, const int32_t* key_lengths, const float* slopes, float scale, void* O, float* LSE,
+                void* workspace, size_t workspace_bytes, void* stream)
 {
     if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
@@ -716,10 +719,32 @@ extern "C" int attn_decode(const void* Q, const void* K, const void* V, int B, i
     const size_t prow = static_cast<size_t>(bh) * decode_split_cap(bh, m) * n;
     p.part_o = num_splits > 1 ? reinterpret_cast<float*>(wsb) : nullptr;
     p.part_ml = num_splits > 1 ? reinterpret_cast<float*>(wsb + round_up(prow * d_k * 4, kWsAlign)) : nullptr;
+    p.slopes = slopes;
     p.status = status;
     p.watchdog_ns = g_watchdog_ns;
     cudaError_t e = attn::launch_decode(d_k, decode_rows(n), tmK, tmV, p, st);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("decode kernel launch", e);
+}
+
+}  // namespace
+
+extern "C" int attn_decode(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
+                           int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O, float* LSE,
+                           void* workspace, size_t workspace_bytes, void* stream)
+{
+    return decode_impl(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, nullptr, scale, O, LSE, workspace,
+                       workspace_bytes, stream);
+}
+
+extern "C" int attn_decode_alibi(const void* Q, const void* K, const void* V, int B, int H, int n, int m,
+                                 int d_k, int d_v, int mask_kind, const int32_t* key_lengths, const float* slopes,
+                                 float scale, void* O, float* LSE, void* workspace, size_t workspace_bytes,
+                                 void* stream)
+{
+    if (slopes == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(slopes, 4)) return ATTN_ERR_MISALIGNED;
+    return decode_impl(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, slopes, scale, O, LSE, workspace,
+                       workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

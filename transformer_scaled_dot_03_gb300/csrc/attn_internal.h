@@ -118,6 +118,7 @@ struct DecodeParams {
     float* LSE;                   // fp32 [B,H,n] or null
     float* part_o;                // fp32 [B*H, num_splits, n, d] (num_splits > 1)
     float* part_ml;               // fp32 [B*H, num_splits, n, 2]: max (log2 domain), sum
+    const float* slopes;          // fp32 [H]: distance-bias slope per head, or null (no bias)
     uint32_t* status;
     uint64_t watchdog_ns;
 };

@@ -19,6 +19,10 @@
 // its partial (max and sum in the log2 domain, unnormalised O, fp32) and a
 // second kernel merges the chunks: M = max_s m_s, L = sum_s l_s 2^(m_s - M),
 // O = sum_s o_s 2^(m_s - M) / L, LSE = (M + log2 L) ln 2.
+//
+// With slopes (the linear distance bias of "第2章：完整的 Transformer 架构" §5.3,
+// ALiBi) each score of row i and key j also gets -m_h |i + (m - n) - j|: one more
+// FMA per score, which the memory-bound kernel absorbs.
 #pragma once
 
 #include <cstdint>
@@ -38,6 +42,7 @@ constexpr int TILE_KEYS = 128;
 constexpr int CHUNK_BYTES = 128 * 64 * 2;   // 128 rows x 64 bf16 columns
 constexpr int NQ_MAX = 8;
 constexpr float LN2 = 0.693147180559945309f;
+constexpr float LOG2E = 1.44269504088896341f;
 
 template <int D>
 struct Layout {
@@ -172,6 +177,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         for (int c = 0; c < CPL; ++c) o[i][c] = 0.f;
     }
     const float sl2 = p.scale_log2;
+    // distance-bias slope of the head in the log2 domain (0: no bias)
+    const float sb = p.slopes != nullptr ? __ldg(p.slopes + bh % p.H) * LOG2E : 0.f;
     const int row = 32 * warp + lane;       // this lane's key row within a tile
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
@@ -214,7 +221,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
             const bool vis = key < j1 && (!mask_is_causal(p.mask) || key <= i + p.causal_off);
-            const float x = vis ? sc[i] * sl2 : -INFINITY;
+            const float x =
+                vis ? fmaf(-sb, fabsf(static_cast<float>(i + p.causal_off - key)), sc[i] * sl2) : -INFINITY;
             float mx = x;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
