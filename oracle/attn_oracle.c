@@ -71,9 +71,11 @@
  * where i' is the query's position among the keys (the n queries are the last
  * n of the m positions, as for the causal mask; i' = i when n = m). The masks,
  * the softmax, the weighted sum and the LSE then proceed as above on these
- * biased scores.
+ * biased scores. The backward (oracle_attn_bwd_alibi) is the chain rule above
+ * with the weights of these biased scores: the bias depends on neither Q nor K,
+ * so the formulas for dS, dQ, dK and dV are unchanged.
  *
- * ORACLE_PLANT (compile-time, default 0, 1..11, 14..16) plants one known mistake so
+ * ORACLE_PLANT (compile-time, default 0, 1..11, 14..17) plants one known mistake so
  * that the test suite can show that its pins catch it; the shipped build never
  * sets it.
  */
@@ -314,8 +316,11 @@ static int run(job_t base)
  */
 static void head_bwd(const double* Qh, const double* Kh, const double* Vh, const double* dOh,
                      int64_t n, int64_t m, int dk, int dv, int mask_kind, int64_t len, double scale,
-                     double* dQh, double* dKh, double* dVh, double* w, double* dp, double* o)
+                     double slope, double* dQh, double* dKh, double* dVh, double* w, double* dp, double* o)
 {
+#if ORACLE_PLANT == 17
+    slope = 0.0;                   /* planted: distance bias dropped in the backward */
+#endif
     for (int64_t t = 0; t < m * dk; ++t) dKh[t] = 0.0;
     for (int64_t t = 0; t < m * dv; ++t) dVh[t] = 0.0;
     for (int64_t i = 0; i < n; ++i) {
@@ -325,7 +330,7 @@ static void head_bwd(const double* Qh, const double* Kh, const double* Vh, const
         double lse;
         for (int c = 0; c < dk; ++c) dq[c] = 0.0;
         /* forward of row i: on return w holds its weights (0 where masked) */
-        attn_row(q, Kh, Vh, m, dk, dv, mask_kind, i, len, m - n, scale, 0.0, w, o, &lse, NULL);
+        attn_row(q, Kh, Vh, m, dk, dv, mask_kind, i, len, m - n, scale, slope, w, o, &lse, NULL);
         if (isinf(lse)) continue;          /* no visible key: o_i = 0 is constant */
         double D = 0.0;
         for (int64_t j = 0; j < m; ++j) {
@@ -368,6 +373,7 @@ typedef struct {
     int64_t B, H, n, m;
     int dk, dv, mask_kind;
     double scale;
+    const double* slopes;  /* per head [H], or NULL: no distance bias */
     double *dQ, *dK, *dV;
     int nthreads, tid;
 } bwd_job_t;
@@ -387,7 +393,8 @@ static void* bwd_worker(void* arg)
             int64_t len = clamp_len(jb->key_lengths, jb->mask_kind, bh / jb->H, jb->m);
             head_bwd(jb->Q + bh * jb->n * jb->dk, jb->K + bh * jb->m * jb->dk,
                      jb->V + bh * jb->m * jb->dv, jb->dO + bh * jb->n * jb->dv, jb->n, jb->m,
-                     jb->dk, jb->dv, jb->mask_kind, len, jb->scale, jb->dQ + bh * jb->n * jb->dk,
+                     jb->dk, jb->dv, jb->mask_kind, len, jb->scale,
+                     jb->slopes ? jb->slopes[bh % jb->H] : 0.0, jb->dQ + bh * jb->n * jb->dk,
                      jb->dK + bh * jb->m * jb->dk, jb->dV + bh * jb->m * jb->dv, w, dp, o);
         }
     }
@@ -463,12 +470,11 @@ int oracle_attn_rows_alibi(const double* Q, const double* K, const double* V, in
     return run(jb);
 }
 
-/* Backward: dQ [B,H,n,dk], dK [B,H,m,dk], dV [B,H,m,dv] for the upstream
- * gradient dO [B,H,n,dv]. Returns 0 on success. */
-int oracle_attn_bwd(const double* Q, const double* K, const double* V, const double* dO,
-                    int64_t B, int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind,
-                    const int32_t* key_lengths, double scale, double* dQ, double* dK, double* dV,
-                    int nthreads)
+/* Backward of every head; slopes may be NULL (no distance bias). */
+static int bwd_impl(const double* Q, const double* K, const double* V, const double* dO, int64_t B,
+                    int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind,
+                    const int32_t* key_lengths, const double* slopes, double scale, double* dQ,
+                    double* dK, double* dV, int nthreads)
 {
     if (bad_args(B, H, n, m, dk, dv, mask_kind)) return -1;
     if (uses_lengths(mask_kind) && key_lengths == NULL) return -1;
@@ -478,7 +484,7 @@ int oracle_attn_bwd(const double* Q, const double* K, const double* V, const dou
     int rc = 0, started = 0;
     for (int t = 0; t < nt; ++t) {
         bwd_job_t jb = {Q, K, V, dO, key_lengths, B, H, n, m, dk, dv, mask_kind, scale,
-                        dQ, dK, dV, nt, t};
+                        slopes, dQ, dK, dV, nt, t};
         jobs[t] = jb;
     }
     if (nt == 1) return bwd_worker(&jobs[0]) == NULL ? 0 : -1;
@@ -492,4 +498,26 @@ int oracle_attn_bwd(const double* Q, const double* K, const double* V, const dou
         if (ret != NULL) rc = -1;
     }
     return rc;
+}
+
+/* Backward: dQ [B,H,n,dk], dK [B,H,m,dk], dV [B,H,m,dv] for the upstream
+ * gradient dO [B,H,n,dv]. Returns 0 on success. */
+int oracle_attn_bwd(const double* Q, const double* K, const double* V, const double* dO,
+                    int64_t B, int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind,
+                    const int32_t* key_lengths, double scale, double* dQ, double* dK, double* dV,
+                    int nthreads)
+{
+    return bwd_impl(Q, K, V, dO, B, H, n, m, dk, dv, mask_kind, key_lengths, NULL, scale, dQ, dK, dV,
+                    nthreads);
+}
+
+/* Backward of the forward with the linear distance bias (slopes [H]). */
+int oracle_attn_bwd_alibi(const double* Q, const double* K, const double* V, const double* dO,
+                          int64_t B, int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind,
+                          const int32_t* key_lengths, const double* slopes, double scale, double* dQ,
+                          double* dK, double* dV, int nthreads)
+{
+    if (slopes == NULL) return -1;
+    return bwd_impl(Q, K, V, dO, B, H, n, m, dk, dv, mask_kind, key_lengths, slopes, scale, dQ, dK, dV,
+                    nthreads);
 }

@@ -75,6 +75,9 @@ def _load(plant: int = 0) -> ctypes.CDLL:
     lib.oracle_attn_rows_alibi.argtypes = [dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p, dp,
                                            ctypes.c_double, i64p, i64, dp, dp, ci]
     lib.oracle_attn_rows_alibi.restype = ci
+    lib.oracle_attn_bwd_alibi.argtypes = [dp, dp, dp, dp, i64, i64, i64, i64, ci, ci, ci, i32p, dp,
+                                          ctypes.c_double, dp, dp, dp, ci]
+    lib.oracle_attn_bwd_alibi.restype = ci
     _libs[plant] = lib
     return lib
 
@@ -183,9 +186,11 @@ def attn_rows(Q, K, V, rows, mask="none", key_lengths=None, scale=None, *, slope
     return O, L
 
 
-def attn_bwd(Q, K, V, dO, mask="none", key_lengths=None, scale=None, *, threads=None, plant=0):
+def attn_bwd(Q, K, V, dO, mask="none", key_lengths=None, scale=None, *, slopes=None, threads=None,
+             plant=0):
     """Oracle backward for the upstream gradient dO [B,H,n,dv]: returns (dQ [B,H,n,dk],
-    dK [B,H,m,dk], dV [B,H,m,dv]) in fp64. ``scale`` defaults to 1/sqrt(d_k)."""
+    dK [B,H,m,dk], dV [B,H,m,dv]) in fp64. ``scale`` defaults to 1/sqrt(d_k); ``slopes``
+    [H] differentiates the forward with the linear distance bias."""
     Qd, Kd, Vd, dOd = _f64(Q), _f64(K), _f64(V), _f64(dO)
     B, H, n, m, dk, dv = _shapes(Qd, Kd, Vd)
     if dOd.shape != (B, H, n, dv):
@@ -195,11 +200,16 @@ def attn_bwd(Q, K, V, dO, mask="none", key_lengths=None, scale=None, *, threads=
     dQ = np.zeros((B, H, n, dk))
     dK = np.zeros((B, H, m, dk))
     dV = np.zeros((B, H, m, dv))
-    rc = _load(plant).oracle_attn_bwd(
-        _ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
-        _ptr(dOd, ctypes.c_double), B, H, n, m, dk, dv, MASK_CODES[mask],
-        _ptr(lens, ctypes.c_int32), sc, _ptr(dQ, ctypes.c_double), _ptr(dK, ctypes.c_double),
-        _ptr(dV, ctypes.c_double), threads or min(default_threads(), 16))
+    sl = _slopes(slopes, H)
+    lib = _load(plant)
+    head = (_ptr(Qd, ctypes.c_double), _ptr(Kd, ctypes.c_double), _ptr(Vd, ctypes.c_double),
+            _ptr(dOd, ctypes.c_double), B, H, n, m, dk, dv, MASK_CODES[mask], _ptr(lens, ctypes.c_int32))
+    tail = (_ptr(dQ, ctypes.c_double), _ptr(dK, ctypes.c_double), _ptr(dV, ctypes.c_double),
+            threads or min(default_threads(), 16))
+    if sl is None:
+        rc = lib.oracle_attn_bwd(*head, sc, *tail)
+    else:
+        rc = lib.oracle_attn_bwd_alibi(*head, _ptr(sl, ctypes.c_double), sc, *tail)
     if rc != 0:
         raise RuntimeError(f"oracle_attn_bwd failed ({rc})")
     return dQ, dK, dV

@@ -5,7 +5,7 @@ head, i' = i + (m - n) the query's position among the keys.
 Each pin raises AssertionError on a mismatch; the tests run them on the shipped
 oracle and on copies with a planted mistake (bias added instead of subtracted,
 query position not aligned for n != m, slope taken per batch entry instead of per
-head), each of which at least one pin must catch.
+head, the bias dropped in the backward), each of which at least one pin must catch.
 """
 
 import math
@@ -120,7 +120,37 @@ def pin_alibi_library(plant=0):
             np.testing.assert_allclose(L, Lt, atol=1e-12)
 
 
-PINS = [pin_alibi_zero_slope, pin_alibi_geometric, pin_alibi_nearest_key, pin_alibi_library]
+def pin_alibi_bwd_finite_differences(plant=0):
+    """The backward of the biased forward: for L = sum(O * G) every entry of dQ, dK, dV
+    equals the central difference of the (pinned) biased forward oracle, h = 1e-6."""
+    h = 1e-6
+    cases = [(1, 2, 4, 4, 2, 2, "causal", None), (1, 2, 3, 5, 2, 3, "none", None),
+             (2, 1, 3, 6, 2, 2, "causal_key_padding", [6, 4])]
+    for t, (B, H, n, m, dk, dv, mask, lens) in enumerate(cases):
+        Q, K, V = rnd((B, H, n, dk), 50 + t), rnd((B, H, m, dk), 60 + t), rnd((B, H, m, dv), 70 + t)
+        G = rnd((B, H, n, dv), 80 + t)
+        slopes = np.array([0.6, 0.15][:H])
+        grads = oracle.attn_bwd(Q, K, V, G, mask, lens, 0.8, slopes=slopes, threads=1, plant=plant)
+
+        def loss():
+            O, _ = oracle.attn_fwd(Q, K, V, mask, lens, 0.8, slopes=slopes, threads=1, plant=plant)
+            return float(np.sum(O * G))
+
+        for x, gx in zip((Q, K, V), grads):
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                lp = loss()
+                x[idx] = old - h
+                lm = loss()
+                x[idx] = old
+                fd[idx] = (lp - lm) / (2 * h)
+            np.testing.assert_allclose(gx, fd, atol=1e-7, err_msg=f"case {t} ({mask})")
+
+
+PINS = [pin_alibi_zero_slope, pin_alibi_geometric, pin_alibi_nearest_key, pin_alibi_library,
+        pin_alibi_bwd_finite_differences]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -128,7 +158,7 @@ def test_pin(pin):
     pin(0)
 
 
-@pytest.mark.parametrize("plant", [14, 15, 16])
+@pytest.mark.parametrize("plant", [14, 15, 16, 17])
 def test_planted_mistake_is_caught(plant):
     caught = []
     for pin in PINS:
