@@ -216,8 +216,8 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     lens_d = x.key_lengths.to(dev) if x.key_lengths is not None else None
     slopes_d = workload_slopes(w).to(dev) if w.alibi else None
-    if w.alibi and (bwd or proj or decode):
-        raise SystemExit("the distance-bias workloads have a forward pass only")
+    if w.alibi and (proj or decode):
+        raise SystemExit("the distance-bias workloads have a forward and a backward pass only")
     dO_h = inputs.make_grad_output(w.B, w.H, w.n, w.d_v, seed=100 + w.seed) if bwd else None
     sets = []
     if proj:
@@ -238,7 +238,11 @@ def run_ours(args):
                   torch.empty(w.B, w.H, w.n, w.d_v, dtype=torch.bfloat16, device=dev),
                   torch.empty(w.B, w.H, w.n, dtype=torch.float32, device=dev)]
             if bwd:
-                attn.attn_fwd(st[0], st[1], st[2], w.mask, lens_d, x.scale, O=st[3], LSE=st[4], stream=stream)
+                if w.alibi:
+                    attn.attn_fwd_alibi(st[0], st[1], st[2], slopes_d, w.mask, lens_d, x.scale, O=st[3], LSE=st[4],
+                                        stream=stream)
+                else:
+                    attn.attn_fwd(st[0], st[1], st[2], w.mask, lens_d, x.scale, O=st[3], LSE=st[4], stream=stream)
                 st += [dO_h.to(dev), torch.empty_like(st[0]), torch.empty_like(st[1]), torch.empty_like(st[2])]
             sets.append(tuple(st))
     if proj:
@@ -265,7 +269,8 @@ def run_ours(args):
             attn.merge_proj(O, Wp, bp, Y=Y, stream=on)
         elif bwd:
             Q, K, V, O, L, dO, dQ, dK, dV = st
-            attn.attn_bwd(Q, K, V, O, L, dO, w.mask, lens, x.scale, dQ, dK, dV, workspace=wsp, stream=on)
+            attn.attn_bwd(Q, K, V, O, L, dO, w.mask, lens, x.scale, dQ, dK, dV, workspace=wsp, stream=on,
+                          slopes=slopes_d)
         elif decode:
             Q, K, V, O, L = st
             attn.attn_decode(Q, K, V, w.mask, lens, x.scale, O=O, LSE=L, workspace=wsp, stream=on)

@@ -113,7 +113,7 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
  *   other arguments as in attn_fwd; supported: d_k == d_v in {64, 128}.
  * Returns ATTN_OK or a negative attn_status_t (INVALID_ARG when slopes is NULL,
  * UNSUPPORTED when d_k != d_v); on error nothing is enqueued. Its decoding
- * form is attn_decode_alibi; attn_bwd takes no bias.
+ * form is attn_decode_alibi, its backward attn_bwd_alibi.
  */
 int attn_fwd_alibi(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
                    int d_v, int mask_kind, const int32_t* key_lengths, const float* slopes, float scale,
@@ -201,6 +201,20 @@ int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const v
              const float* LSE, int B, int H, int n, int m, int d_k, int d_v, int mask_kind,
              const int32_t* key_lengths, float scale, void* dQ, void* dK, void* dV,
              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_bwd for the forward with the linear distance bias (attn_fwd_alibi,
+ * "第2章：完整的 Transformer 架构" §5.3): P is recomputed from the biased scores
+ * and the biased forward's LSE; the bias depends on neither Q nor K, so the
+ * formulas for dQ, dK and dV are those of attn_bwd. `slopes` as in
+ * attn_fwd_alibi (device fp32 [H], 4-byte aligned); O and LSE must come from
+ * attn_fwd_alibi with the same slopes. Workspace, results and status codes as in
+ * attn_bwd; ATTN_ERR_INVALID_ARG when slopes is NULL.
+ */
+int attn_bwd_alibi(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* LSE, int B, int H, int n, int m, int d_k, int d_v, int mask_kind,
+                   const int32_t* key_lengths, const float* slopes, float scale, void* dQ, void* dK,
+                   void* dV, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Attention forward for a few query rows against a long key/value sequence:

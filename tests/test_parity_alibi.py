@@ -1,7 +1,7 @@
 """GPU parity of the forward with the linear distance bias ("第2章：完整的 Transformer
 架构" §5.3, ALiBi) against the fp64 oracle, element by element, on seeded bf16
-inputs, through the C entry points attn_fwd_alibi and attn_decode_alibi (the
-few-row decoding form).
+inputs, through the C entry points attn_fwd_alibi, attn_decode_alibi (the
+few-row decoding form) and attn_bwd_alibi (its gradients).
 
 The bias makes the nearby keys dominate a row, so rows are sharper than without
 it and |O| approaches the largest |v_j|. The comparison therefore uses the
@@ -190,4 +190,62 @@ def test_decode_rejects_null_slopes():
     rc = lib.attn_decode_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), 1, 1, 1, 1, 64, 64, 0, None,
                                None, ctypes.c_float(-1.0), vp(q.data_ptr()), None, None, ctypes.c_size_t(0),
                                vp(torch.cuda.current_stream().cuda_stream))
+    assert rc == attn.ATTN_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ backward (attn_bwd_alibi)
+#
+# The GPU differentiates from its own biased forward (bf16 O, fp32 LSE); the bound
+# is the backward's (tests/test_bwd_parity.py) with the weights of the biased
+# scores: |G - G_ref| <= 2 bound + 1e-6 elementwise, u = 2^-8,
+#   dV: u |dV_ref| + u Wᵀ|dO|;  dK: u |dK_ref| + scale Tᵀ|Q|;  dQ: u |dQ_ref| + scale T|K|,
+#   T = W (u |dP - D| + E),  E_i = u sum_c |dO_ic| (|O_ic| + A_ic).
+
+def check_bwd(x, slopes, label):
+    B, H, n, d = x.Q.shape
+    dO = inputs.make_grad_output(B, H, n, x.V.shape[3], seed=77)
+    Q, K, V, g, sl = x.Q.cuda(), x.K.cuda(), x.V.cuda(), dO.cuda(), slopes.cuda()
+    lens = x.key_lengths.cuda() if x.key_lengths is not None else None
+    O, LSE = attn.attn_fwd_alibi(Q, K, V, sl, x.mask, lens, x.scale)
+    got = attn.attn_bwd(Q, K, V, O, LSE, g, x.mask, lens, x.scale, slopes=sl)
+    rc, detail = attn.device_status()
+    assert rc == attn.ATTN_OK, (rc, detail)
+    got = [t.float().cpu().numpy() for t in got]
+    refs = oracle.attn_bwd(x.Q, x.K, x.V, dO, x.mask, x.key_lengths, x.scale, slopes=slopes)
+    Qd, Kd, Vd, gd = (t.double().numpy() for t in (x.Q, x.K, x.V, dO))
+    Or, _, W = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale, slopes=slopes, weights=True)
+    A, _ = oracle.attn_fwd(x.Q, x.K, x.V.abs(), x.mask, x.key_lengths, x.scale, slopes=slopes)
+    dP = np.einsum("bhic,bhjc->bhij", gd, Vd)
+    D = np.sum(gd * Or, axis=-1)
+    E = BF16_U * np.sum(np.abs(gd) * (np.abs(Or) + A), axis=-1)
+    T = W * (BF16_U * np.abs(dP - D[..., None]) + E[..., None])
+    dQr, dKr, dVr = refs
+    bds = (BF16_U * np.abs(dQr) + x.scale * np.einsum("bhij,bhjc->bhic", T, np.abs(Kd)),
+           BF16_U * np.abs(dKr) + x.scale * np.einsum("bhij,bhic->bhjc", T, np.abs(Qd)),
+           BF16_U * np.abs(dVr) + BF16_U * np.einsum("bhij,bhic->bhjc", W, np.abs(gd)))
+    for name, G, R, bd in zip(("dQ", "dK", "dV"), got, refs, bds):
+        assert np.all(np.isfinite(G)), f"{label}: non-finite {name}"
+        excess = np.abs(G - R) - (2 * bd + 1e-6)
+        assert excess.max() <= 0, f"{label}: {name} exceeds its bound by {excess.max():.3e}"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("mask,n,m", [("none", 200, 200), ("causal", 256, 256), ("causal", 130, 300),
+                                      ("key_padding", 150, 260), ("causal_key_padding", 200, 200)])
+def test_bwd(d, mask, n, m):
+    lens = [m, m // 2, 1] if mask in inputs.LENGTH_MASKS else None
+    B = 3 if lens else 2
+    x = inputs.make_inputs(B, 4, n, m, d, d, mask, seed=5500 + n + m + d, key_lengths=lens)
+    check_bwd(x, inputs.alibi_slopes(4), f"bwd {mask} n={n} m={m} d={d}")
+
+
+def test_bwd_rejects_null_slopes():
+    lib = attn.load()
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 1, 4, device="cuda")
+    vp = ctypes.c_void_p
+    rc = lib.attn_bwd_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()),
+                            vp(lse.data_ptr()), 1, 1, 4, 4, 64, 64, 0, None, None, ctypes.c_float(-1.0),
+                            vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), None, ctypes.c_size_t(0),
+                            vp(torch.cuda.current_stream().cuda_stream))
     assert rc == attn.ATTN_ERR_INVALID_ARG

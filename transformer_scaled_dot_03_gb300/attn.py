@@ -32,7 +32,7 @@ MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PAD
               _inputs.MASK_CAUSAL_KEY_PADDING: 3}
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_fwd", "attn_fwd_alibi", "attn_decode_alibi", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
+EXPORTS = ("attn_fwd", "attn_fwd_alibi", "attn_decode_alibi", "attn_bwd_alibi", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
            "attn_last_error", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
            "attn_decode_workspace_size", "attn_proj_heads", "attn_merge_proj")
 
@@ -70,6 +70,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32,
                                  vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.attn_bwd.restype = i32
+        lib.attn_bwd_alibi.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, f32,
+                                       vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.attn_bwd_alibi.restype = i32
         lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
         lib.attn_decode.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp,
@@ -205,10 +208,13 @@ def bwd_workspace_size(B, H, n, m, d_k, d_v) -> int:
 def attn_bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor, LSE: torch.Tensor,
              dO: torch.Tensor, mask: str = "none", key_lengths: torch.Tensor | None = None,
              scale: float | None = None, dQ: torch.Tensor | None = None, dK: torch.Tensor | None = None,
-             dV: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+             dV: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None,
+             slopes: torch.Tensor | None = None):
     """Attention backward on the GPU: (dQ, dK, dV) bf16 for the upstream gradient dO, given
     the forward's inputs Q, K, V and outputs O (bf16) and LSE (fp32). ``workspace`` (uint8
     CUDA tensor of at least ``bwd_workspace_size`` bytes) is allocated here when omitted.
+    ``slopes`` (contiguous fp32 CUDA [H]) differentiates ``attn_fwd_alibi`` with those
+    slopes (attn_bwd_alibi).
     Asynchronous on ``stream`` (default: PyTorch's current stream)."""
     if mask not in MASK_CODES:
         raise ValueError(f"unknown mask {mask!r}")
@@ -239,10 +245,18 @@ def attn_bwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor,
     elif workspace.numel() < ws_bytes or workspace.dtype != torch.uint8 or not workspace.is_cuda:
         raise ValueError(f"workspace must be a uint8 CUDA tensor of at least {ws_bytes} bytes")
     sc = -1.0 if scale is None else float(scale)
-    rc = attn_bwd_raw(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), B, H, n, m, d_k, d_v,
-                      MASK_CODES[mask], _ptr(key_lengths) if uses_lengths else None, sc,
-                      _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace), workspace.numel(),
-                      _stream_handle(stream))
+    lens_p = _ptr(key_lengths) if uses_lengths else None
+    if slopes is None:
+        rc = attn_bwd_raw(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), B, H, n, m, d_k, d_v,
+                          MASK_CODES[mask], lens_p, sc, _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
+                          workspace.numel(), _stream_handle(stream))
+    else:
+        if slopes.dtype != torch.float32 or not slopes.is_cuda or slopes.numel() != H or not slopes.is_contiguous():
+            raise ValueError("slopes must be a contiguous fp32 CUDA tensor with one value per head")
+        rc = load().attn_bwd_alibi(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), int(B), int(H), int(n),
+                                   int(m), int(d_k), int(d_v), MASK_CODES[mask], lens_p, _ptr(slopes),
+                                   ctypes.c_float(sc), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(workspace),
+                                   ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(_stream_handle(stream)))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd", last_error() if rc == ATTN_ERR_CUDA else "")
     return dQ, dK, dV

@@ -511,10 +511,12 @@ extern "C" size_t attn_bwd_workspace_size(int B, int H, int n, int m, int d_k, i
     return bwd_workspace(static_cast<int64_t>(B) * H, n, d_k).total;
 }
 
-extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                        const float* LSE, int B, int H, int n, int m, int d_k, int d_v, int mask_kind,
-                        const int32_t* key_lengths, float scale, void* dQ, void* dK, void* dV, void* workspace,
-                        size_t workspace_bytes, void* stream)
+namespace {
+
+// The backward; `slopes` (device fp32 [H]) for the forward with the linear distance bias, null without.
+int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE, int B,
+             int H, int n, int m, int d_k, int d_v, int mask_kind, const int32_t* key_lengths, const float* slopes,
+             float scale, void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, void* stream)
 {
     if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_KEY_PADDING) return ATTN_ERR_INVALID_ARG;
@@ -586,6 +588,7 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
     p.dV = dV;
     p.scale_log2 = static_cast<float>(sc * 1.4426950408889634074);
     p.scale = static_cast<float>(sc);
+    p.slopes = slopes;
     p.status = status;
     p.watchdog_ns = g_watchdog_ns;
     p.debug_flags = g_debug_flags;
@@ -596,11 +599,36 @@ extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void*
                                      0, st, static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), LSE,
                                      bh, n, ws.n_pad, d_v, lse2, dd, reinterpret_cast<float4*>(dq_acc), dq_vec);
     if (e != cudaSuccess) return fail_cuda("backward preparation kernel launch", e);
-    e = d_k == 64 ? attn::launch_bwd_d64(mask_kind, maps, p, st) : attn::launch_bwd_d128(mask_kind, maps, p, st);
+    if (slopes != nullptr)
+        e = attn::launch_bwd_alibi(d_k, mask_kind, maps, p, st);
+    else
+        e = d_k == 64 ? attn::launch_bwd_d64(mask_kind, maps, p, st) : attn::launch_bwd_d128(mask_kind, maps, p, st);
     if (e != cudaSuccess) return fail_cuda("backward kernel launch", e);
     e = attn::launch_pdl(bwd_convert_kernel, dim3(static_cast<unsigned>(grid_for(dq_vec, 256))), dim3(256), 0, st,
                          reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(dQ), dq_vec, p.scale);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("dQ conversion kernel launch", e);
+}
+
+}  // namespace
+
+extern "C" int attn_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                        const float* LSE, int B, int H, int n, int m, int d_k, int d_v, int mask_kind,
+                        const int32_t* key_lengths, float scale, void* dQ, void* dK, void* dV, void* workspace,
+                        size_t workspace_bytes, void* stream)
+{
+    return bwd_impl(Q, K, V, O, dO, LSE, B, H, n, m, d_k, d_v, mask_kind, key_lengths, nullptr, scale, dQ, dK, dV,
+                    workspace, workspace_bytes, stream);
+}
+
+extern "C" int attn_bwd_alibi(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                              const float* LSE, int B, int H, int n, int m, int d_k, int d_v, int mask_kind,
+                              const int32_t* key_lengths, const float* slopes, float scale, void* dQ, void* dK,
+                              void* dV, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (slopes == nullptr) return ATTN_ERR_INVALID_ARG;
+    if (!aligned(slopes, 4)) return ATTN_ERR_MISALIGNED;
+    return bwd_impl(Q, K, V, O, dO, LSE, B, H, n, m, d_k, d_v, mask_kind, key_lengths, slopes, scale, dQ, dK, dV,
+                    workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -92,6 +92,7 @@ struct BwdParams {
     void* dV;
     float scale_log2;             // scale * log2(e)
     float scale;
+    const float* slopes;          // fp32 [H]: distance-bias slope per head (bias kernels only)
     uint32_t* status;
     uint64_t watchdog_ns;
     uint32_t debug_flags;
@@ -103,6 +104,8 @@ struct BwdMaps {
 
 cudaError_t launch_bwd_d64(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_d128(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+// Backward with the linear distance bias (p.slopes), d_k = d_v = d in {64, 128}.
+cudaError_t launch_bwd_alibi(int d, int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 
 // Few-row forward (attn_kernel_decode.cuh): one CTA per (b, h, key chunk).
 struct DecodeParams {

@@ -101,7 +101,7 @@ __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, uint64_t li
     return true;
 }
 
-template <int D, int MASK>
+template <int D, int MASK, bool BIAS>
 __global__ void __launch_bounds__(Layout<D>::NUM_THREADS, 1)
 attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 {
@@ -299,6 +299,7 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         const int key = k0 + r;
         const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
         const float sl2 = p.scale_log2;
+        const float sb = BIAS ? __ldg(p.slopes + bh % p.H) * 1.44269504088896341f : 0.f;   // log2 domain
         bool ok = true;
         bool store_pending = false;
         // Rendezvous of the eight compute warps through an mbarrier (every thread
@@ -343,7 +344,9 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             tmem_ld32(tmem + lane_base + L::DP_COL + c0, dr);
             tmem_ld32(tmem + lane_base + L::DP_COL + c0 + 32, dr + 32);
             tmem_wait_ld();
-            // P = exp2(S·scale·log2 e − LSE·log2 e)
+            // P = exp2(S·scale·log2 e − LSE·log2 e), with the distance bias
+            // −sb |i' − key| of query column j (i' = q0 + c0 + j + m − n) under BIAS
+            const float d1 = static_cast<float>(q0 + c0 + p.causal_off - key);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float lz[32];
@@ -352,7 +355,8 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int j = 32 * c + i;
-                    sr[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, -lz[i])));
+                    const float z = BIAS ? fmaf(-sb, fabsf(d1 + static_cast<float>(j)), -lz[i]) : -lz[i];
+                    sr[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, z)));
                 }
             }
             if (need_mask) {
@@ -650,7 +654,7 @@ struct BwdCursor {
     }
 };
 
-template <int MASK>
+template <int MASK, bool BIAS>
 __global__ void __launch_bounds__(LayoutPipe::NUM_THREADS, 1)
 attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 {
@@ -938,6 +942,7 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     continue;
                 }
                 const int key = w.k0 + r;
+                const float sb = BIAS ? __ldg(p.slopes + w.bh % p.H) * 1.44269504088896341f : 0.f;   // log2 domain
                 for (int t = 0; ok && t < w.nt; ++t) {
                     const int s = gt % L::QS;
                     const uint32_t parity = static_cast<uint32_t>(gt) & 1u;
@@ -959,6 +964,7 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     mbar_arrive(bar(L::B_RDONE));    // the MMA warp may compute the next Sᵀ, dPᵀ
                     const uint32_t lse_s = sbase + L::LSE_OFF + (s * BM + c0) * 4;
                     const uint32_t dd_s = sbase + L::DD_OFF + (s * BM + c0) * 4;
+                    const float d1 = static_cast<float>(q0 + c0 + p.causal_off - key);
                     const bool need_mask =
                         __any_sync(0xffffffffu, key >= w.kv_len || q0 + c0 + 63 >= p.n ||
                                                     (mask_is_causal(MASK) && key > q0 + c0 + p.causal_off));
@@ -970,7 +976,9 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const int j = 32 * c + i;
-                            sr[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, -lz[i])));
+                            // with the distance bias −sb |i' − key| of query column j under BIAS
+                            const float z = BIAS ? fmaf(-sb, fabsf(d1 + static_cast<float>(j)), -lz[i]) : -lz[i];
+                            sr[j] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(sr[j]), sl2, z)));
                         }
                     }
                     if (need_mask) {
@@ -1099,11 +1107,11 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     }
 }
 
-template <int D, int MASK>
+template <int D, int MASK, bool BIAS = false>
 cudaError_t launch(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream)
 {
     using L = typename std::conditional<D == 64, LayoutPipe, Layout<D>>::type;
-    auto kern = D == 64 ? attn_bwd_pipe_kernel<MASK> : attn_bwd_kernel<D, MASK>;
+    auto kern = D == 64 ? attn_bwd_pipe_kernel<MASK, BIAS> : attn_bwd_kernel<D, MASK, BIAS>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
