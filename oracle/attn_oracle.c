@@ -31,6 +31,11 @@
  *           causal and   both conditions             ("Transformer 详解" §5.3:
  *           key padding                               tgt_mask = pad_mask &
  *                                                     subsequent_mask)
+ *           causal in    j < len_b and               (a cache of fixed size m
+ *           the cache    j <= i + (len_b - n)         filled to len_b positions,
+ *                                                     the n queries being its
+ *                                                     last n: the wiki page's KV
+ *                                                     cache, "实现要点")
  *   mu    = max_{j in J} s_j;  Z = sum_{j in J} exp(s_j - mu)
  *   w_j   = exp(s_j - mu) / Z for j in J, 0 otherwise      (row softmax; the
  *           shift by mu leaves the value unchanged and keeps exp in range)
@@ -75,7 +80,7 @@
  * with the weights of these biased scores: the bias depends on neither Q nor K,
  * so the formulas for dS, dQ, dK and dV are unchanged.
  *
- * ORACLE_PLANT (compile-time, default 0, 1..11, 14..17) plants one known mistake so
+ * ORACLE_PLANT (compile-time, default 0, 1..11, 14..18) plants one known mistake so
  * that the test suite can show that its pins catch it; the shipped build never
  * sets it.
  */
@@ -93,7 +98,8 @@ enum {
     ORACLE_MASK_NONE = 0,
     ORACLE_MASK_CAUSAL = 1,
     ORACLE_MASK_KEY_PADDING = 2,
-    ORACLE_MASK_CAUSAL_KEY_PADDING = 3
+    ORACLE_MASK_CAUSAL_KEY_PADDING = 3,
+    ORACLE_MASK_CAUSAL_CACHE = 4
 };
 
 static int causal_visible(int64_t i, int64_t j, int64_t off)
@@ -126,6 +132,7 @@ static int visible(int mask_kind, int64_t i, int64_t j, int64_t len, int64_t off
     switch (mask_kind) {
     case ORACLE_MASK_CAUSAL: return causal_visible(i, j, off);
     case ORACLE_MASK_KEY_PADDING: return padding_visible(i, j, len);
+    case ORACLE_MASK_CAUSAL_CACHE: return causal_visible(i, j, off) && padding_visible(i, j, len);
     case ORACLE_MASK_CAUSAL_KEY_PADDING:
 #if ORACLE_PLANT == 8
         return causal_visible(i, j, off) || padding_visible(i, j, len);  /* planted: union */
@@ -138,7 +145,21 @@ static int visible(int mask_kind, int64_t i, int64_t j, int64_t len, int64_t off
 
 static int uses_lengths(int mask_kind)
 {
-    return mask_kind == ORACLE_MASK_KEY_PADDING || mask_kind == ORACLE_MASK_CAUSAL_KEY_PADDING;
+    return mask_kind == ORACLE_MASK_KEY_PADDING || mask_kind == ORACLE_MASK_CAUSAL_KEY_PADDING ||
+           mask_kind == ORACLE_MASK_CAUSAL_CACHE;
+}
+
+/* Offset of row i's position among the keys: the n queries are the last n of the m
+ * keys, or of the first len keys under the cache mask (position i + off). */
+static int64_t row_offset(int mask_kind, int64_t m, int64_t n, int64_t len)
+{
+#if ORACLE_PLANT == 18
+    (void)mask_kind;
+    (void)len;
+    return m - n;                  /* planted: cache mask aligned to m, not to the length */
+#else
+    return mask_kind == ORACLE_MASK_CAUSAL_CACHE ? len - n : m - n;
+#endif
 }
 
 static int64_t clamp_len(const int32_t* key_lengths, int mask_kind, int64_t b, int64_t m)
@@ -264,7 +285,8 @@ static void* worker(void* arg)
             for (int64_t i = 0; i < jb->n; ++i) {
                 int64_t r = bh * jb->n + i;
                 attn_row(jb->Q + r * jb->dk, Kh, Vh, jb->m, jb->dk, jb->dv, jb->mask_kind, i,
-                         len, jb->m - jb->n, jb->scale, slope, s, jb->O + r * jb->dv, jb->LSE + r,
+                         len, row_offset(jb->mask_kind, jb->m, jb->n, len), jb->scale, slope, s,
+                         jb->O + r * jb->dv, jb->LSE + r,
                          jb->W ? jb->W + r * jb->m : NULL);
             }
         }
@@ -276,7 +298,7 @@ static void* worker(void* arg)
             int64_t len = clamp_len(jb->key_lengths, jb->mask_kind, b, jb->m);
             attn_row(jb->Q + r * jb->dk, jb->K + bh * jb->m * jb->dk,
                      jb->V + bh * jb->m * jb->dv, jb->m, jb->dk, jb->dv, jb->mask_kind, i, len,
-                     jb->m - jb->n, jb->scale, head_slope(jb, b, bh % jb->H), s,
+                     row_offset(jb->mask_kind, jb->m, jb->n, len), jb->scale, head_slope(jb, b, bh % jb->H), s,
                      jb->O + k * jb->dv, jb->LSE + k, NULL);
         }
     }
@@ -330,7 +352,8 @@ static void head_bwd(const double* Qh, const double* Kh, const double* Vh, const
         double lse;
         for (int c = 0; c < dk; ++c) dq[c] = 0.0;
         /* forward of row i: on return w holds its weights (0 where masked) */
-        attn_row(q, Kh, Vh, m, dk, dv, mask_kind, i, len, m - n, scale, slope, w, o, &lse, NULL);
+        attn_row(q, Kh, Vh, m, dk, dv, mask_kind, i, len, row_offset(mask_kind, m, n, len), scale, slope, w, o,
+                 &lse, NULL);
         if (isinf(lse)) continue;          /* no visible key: o_i = 0 is constant */
         double D = 0.0;
         for (int64_t j = 0; j < m; ++j) {
@@ -407,7 +430,7 @@ static void* bwd_worker(void* arg)
 static int bad_args(int64_t B, int64_t H, int64_t n, int64_t m, int dk, int dv, int mask_kind)
 {
     return B < 0 || H < 0 || n < 0 || m < 0 || dk < 1 || dv < 1 || mask_kind < 0 ||
-           mask_kind > 3;
+           mask_kind > 4;
 }
 
 /* Full forward: O [B,H,n,dv] and LSE [B,H,n]. W (optional, [B,H,n,m]) gets the

@@ -23,7 +23,7 @@ SRC = os.path.join(HERE, "attn_oracle.c")
 BUILD_DIR = os.path.join(HERE, "_build")
 
 # The oracle's own mask codes (independent of the CUDA library's enum).
-MASK_CODES = {"none": 0, "causal": 1, "key_padding": 2, "causal_key_padding": 3}
+MASK_CODES = {"none": 0, "causal": 1, "key_padding": 2, "causal_key_padding": 3, "causal_cache": 4}
 
 _lock = threading.Lock()
 _libs: dict[int, ctypes.CDLL] = {}

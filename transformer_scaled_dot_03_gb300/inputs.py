@@ -27,8 +27,10 @@ MASK_NONE = "none"
 MASK_CAUSAL = "causal"
 MASK_KEY_PADDING = "key_padding"
 MASK_CAUSAL_KEY_PADDING = "causal_key_padding"
-MASK_KINDS = (MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING)
-LENGTH_MASKS = (MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING)
+MASK_CAUSAL_CACHE = "causal_cache"     # causal, the queries being the last n of each entry's key_lengths[b]
+MASK_KINDS = (MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING, MASK_CAUSAL_CACHE)
+LENGTH_MASKS = (MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING, MASK_CAUSAL_CACHE)
+CAUSAL_MASKS = (MASK_CAUSAL, MASK_CAUSAL_KEY_PADDING, MASK_CAUSAL_CACHE)
 
 
 def nominal_pairs(n: int, m: int, mask: str) -> float:
@@ -36,7 +38,7 @@ def nominal_pairs(n: int, m: int, mask: str) -> float:
     visible part with the masked triangle counted as half its square (n*m - n*n/2
     for n <= m, m*m/2 for n > m), the usual convention that charges a square
     causal mask n*m/2."""
-    if mask not in (MASK_CAUSAL, MASK_CAUSAL_KEY_PADDING):
+    if mask not in CAUSAL_MASKS:
         return float(n) * m
     if n <= m:
         return float(n) * m - float(n) * n / 2
