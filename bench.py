@@ -464,6 +464,11 @@ def effective_flops(w, x):
     """FLOPs of the (query, key) pairs the masks leave visible, counted exactly with
     the drawn key lengths: 2*(d_k + d_v) per pair."""
     i = torch.arange(w.n, dtype=torch.float64)
+    if w.mask == inputs.MASK_CAUSAL_CACHE:
+        # keys j < len_b with j <= i + len_b - n
+        lens = x.key_lengths.to(torch.float64).clamp(0, w.m)
+        pairs = float((i[None, :] + lens[:, None] - w.n + 1).clamp(min=0).minimum(lens[:, None]).sum()) * w.H
+        return 2.0 * (w.d_k + w.d_v) * pairs
     if w.mask in (inputs.MASK_CAUSAL, inputs.MASK_CAUSAL_KEY_PADDING):
         per_row_cap = (i + (w.m - w.n) + 1).clamp(0, w.m)      # keys j <= i + m - n
     else:

@@ -25,6 +25,14 @@
  *                            both conditions at once (the decoder target mask
  *                            of "Transformer 详解" §5.3: pad mask AND
  *                            subsequent mask).
+ *     ATTN_MASK_CAUSAL_CACHE causal inside a partly filled key/value cache: m
+ *                            slots of which key_lengths[b] are filled, the n
+ *                            queries being the last n filled positions, so key
+ *                            j is visible to query i iff j < key_lengths[b] and
+ *                            j <= i + (key_lengths[b] - n) (the cache of fixed
+ *                            size with batched entries of the transformer wiki
+ *                            page's KV cache section; with key_lengths[b] = m
+ *                            it is ATTN_MASK_CAUSAL).
  * A row that sees no key gets O = 0 and LSE = -inf.
  * The n x m score matrix is never written to memory. LSE is the per-row
  * natural-log normaliser (not printed on the pages; a standard by-product
@@ -59,7 +67,8 @@ typedef enum {
     ATTN_MASK_NONE = 0,
     ATTN_MASK_CAUSAL = 1,
     ATTN_MASK_KEY_PADDING = 2,
-    ATTN_MASK_CAUSAL_KEY_PADDING = 3
+    ATTN_MASK_CAUSAL_KEY_PADDING = 3,
+    ATTN_MASK_CAUSAL_CACHE = 4
 } attn_mask_kind_t;
 
 typedef enum {
@@ -81,8 +90,8 @@ typedef enum {
  *                is a no-op; m = 0 writes O = 0 and LSE = -inf.
  *   d_k, d_v     head dims, each 64 or 128 (d_k != d_v allowed).
  *   mask_kind    attn_mask_kind_t.
- *   key_lengths  device int32 [B]; required for KEY_PADDING and
- *                CAUSAL_KEY_PADDING, ignored otherwise.
+ *   key_lengths  device int32 [B]; required for KEY_PADDING,
+ *                CAUSAL_KEY_PADDING and CAUSAL_CACHE, ignored otherwise.
  *                Values are read on the device and clamped to [0, m]; a length
  *                of 0 gives O = 0 and LSE = -inf for every row of that entry.
  *   scale        multiplies q.k; a value <= 0, NaN or inf selects 1/sqrt(d_k)
@@ -221,9 +230,11 @@ int attn_bwd_alibi(const void* Q, const void* K, const void* V, const void* O, c
  * the decoding step of a model that keeps its keys and values in a cache
  * (each new token's query attends to every cached position). Same operation,
  * masks, layouts and results as attn_fwd (any n <= 8 gives the same O and LSE
- * up to rounding); the implementation streams K and V once from memory with a
- * split over the keys instead of the tensor-core tiles of attn_fwd, which pays
- * off when n is small.
+ * up to rounding). With few (b, h) pairs for the GPU (B*H below four per CTA
+ * slot: 4 x SMs at d = 128, 8 x SMs at d = 64) it streams K and V once with a
+ * split over the keys and merges the chunks; with more pairs it runs the
+ * tensor-core kernel of attn_fwd, which then streams K and V at the memory
+ * system's rate without a merge.
  *   n            1..8 query rows per (b, h); 0 is a no-op; more is
  *                ATTN_ERR_UNSUPPORTED (use attn_fwd).
  *   d_k, d_v     equal, 64 or 128.

@@ -57,7 +57,8 @@ def call(Q=P, K=P, V=P, B=1, H=1, n=4, m=4, dk=64, dv=64, mask=0, lens=None, O=P
     (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
     (dict(n=-3), attn.ATTN_ERR_INVALID_ARG),
     (dict(m=-1), attn.ATTN_ERR_INVALID_ARG),
-    (dict(mask=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=4), attn.ATTN_ERR_INVALID_ARG),          # the cache mask without key lengths
     (dict(mask=-1), attn.ATTN_ERR_INVALID_ARG),
     (dict(mask=2, lens=None), attn.ATTN_ERR_INVALID_ARG),         # key padding needs lengths
     (dict(mask=3, lens=None), attn.ATTN_ERR_INVALID_ARG),
@@ -113,7 +114,8 @@ def call_bwd(B=1, H=1, n=4, m=4, dk=64, dv=64, mask=0, lens=None, dQ=P2, dK=P2, 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
-    (dict(mask=4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=5), attn.ATTN_ERR_INVALID_ARG),
+    (dict(mask=4), attn.ATTN_ERR_INVALID_ARG),          # the cache mask without key lengths
     (dict(mask=2, lens=None), attn.ATTN_ERR_INVALID_ARG),
     (dict(mask=3, lens=None), attn.ATTN_ERR_INVALID_ARG),
     (dict(dk=64, dv=128), attn.ATTN_ERR_UNSUPPORTED),

@@ -29,7 +29,7 @@ ATTN_ERR_CUDA = -4
 ATTN_ERR_TIMEOUT = -5
 
 MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PADDING: 2,
-              _inputs.MASK_CAUSAL_KEY_PADDING: 3}
+              _inputs.MASK_CAUSAL_KEY_PADDING: 3, _inputs.MASK_CAUSAL_CACHE: 4}
 
 # Every symbol include/attn.h declares.
 EXPORTS = ("attn_fwd", "attn_fwd_alibi", "attn_decode_alibi", "attn_bwd_alibi", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",

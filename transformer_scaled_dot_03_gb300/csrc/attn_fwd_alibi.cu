@@ -14,6 +14,7 @@ static cudaError_t launch_bias(int mask, const TensorMaps& maps, const FwdParams
     case MASK_CAUSAL: return dp::launch<D, D, MASK_CAUSAL, true>(maps, p, num_sms, stream);
     case MASK_KEY_PADDING: return dp::launch<D, D, MASK_KEY_PADDING, true>(maps, p, num_sms, stream);
     case MASK_CAUSAL_KEY_PADDING: return dp::launch<D, D, MASK_CAUSAL_KEY_PADDING, true>(maps, p, num_sms, stream);
+    case MASK_CAUSAL_CACHE: return dp::launch<D, D, MASK_CAUSAL_CACHE, true>(maps, p, num_sms, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -25,6 +25,7 @@ static cudaError_t launch_dp(int mask, const TensorMaps& maps, const FwdParams& 
     case MASK_KEY_PADDING: return dp::launch<64, 64, MASK_KEY_PADDING>(maps, p, num_sms, stream);
     case MASK_CAUSAL_KEY_PADDING:
         return dp::launch<64, 64, MASK_CAUSAL_KEY_PADDING>(maps, p, num_sms, stream);
+    case MASK_CAUSAL_CACHE: return dp::launch<64, 64, MASK_CAUSAL_CACHE>(maps, p, num_sms, stream);
     default: return cudaErrorInvalidValue;
     }
 }

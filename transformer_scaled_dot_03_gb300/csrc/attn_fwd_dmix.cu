@@ -13,6 +13,7 @@ static cudaError_t launch_mix(int mask, const TensorMaps& maps, const FwdParams&
     case MASK_CAUSAL: return dp::launch<DK, DV, MASK_CAUSAL>(maps, p, num_sms, stream);
     case MASK_KEY_PADDING: return dp::launch<DK, DV, MASK_KEY_PADDING>(maps, p, num_sms, stream);
     case MASK_CAUSAL_KEY_PADDING: return dp::launch<DK, DV, MASK_CAUSAL_KEY_PADDING>(maps, p, num_sms, stream);
+    case MASK_CAUSAL_CACHE: return dp::launch<DK, DV, MASK_CAUSAL_CACHE>(maps, p, num_sms, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -8,15 +8,22 @@
 
 namespace attn {
 
-enum { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_KEY_PADDING = 2, MASK_CAUSAL_KEY_PADDING = 3 };
+enum { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_KEY_PADDING = 2, MASK_CAUSAL_KEY_PADDING = 3, MASK_CAUSAL_CACHE = 4 };
 
 __host__ __device__ constexpr bool mask_is_causal(int mask)
 {
-    return mask == MASK_CAUSAL || mask == MASK_CAUSAL_KEY_PADDING;
+    return mask == MASK_CAUSAL || mask == MASK_CAUSAL_KEY_PADDING || mask == MASK_CAUSAL_CACHE;
 }
 __host__ __device__ constexpr bool mask_has_lengths(int mask)
 {
-    return mask == MASK_KEY_PADDING || mask == MASK_CAUSAL_KEY_PADDING;
+    return mask == MASK_KEY_PADDING || mask == MASK_CAUSAL_KEY_PADDING || mask == MASK_CAUSAL_CACHE;
+}
+// Offset of a query row's position among the keys (row i sits at i + offset): the
+// n queries are the last n of the m keys, or of the kv_len filled keys of each
+// entry's cache under MASK_CAUSAL_CACHE.
+__host__ __device__ constexpr int causal_offset(int mask, int m_minus_n, int kv_len, int n)
+{
+    return mask == MASK_CAUSAL_CACHE ? kv_len - n : m_minus_n;
 }
 
 // Bits of the device status word: which bounded wait gave up.

@@ -128,10 +128,11 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         return;
     }
     // query tiles that can see this key tile
+    const int off = causal_offset(MASK, p.causal_off, kv_len, p.n);   // row i sits at key position i + off
     const int nqb = (p.n + BM - 1) / BM;
     int qb_lo = 0;
     if (mask_is_causal(MASK)) {
-        const int first_q = k0 - p.causal_off;     // first row that sees key k0
+        const int first_q = k0 - off;              // first row that sees key k0
         qb_lo = first_q <= 0 ? 0 : first_q / BM;
     }
     const int nt = nqb - qb_lo;                    // >= 1: the last row sees every key < kv_len
@@ -336,7 +337,7 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             const uint32_t dd_s = sbase + L::DD_OFF + (s * BM + c0) * 4;
             const bool need_mask =
                 __any_sync(0xffffffffu, key >= kv_len || q0 + c0 + 63 >= p.n ||
-                                            (mask_is_causal(MASK) && key > q0 + c0 + p.causal_off));
+                                            (mask_is_causal(MASK) && key > q0 + c0 + off));
             // this warpgroup's half of the row of Sᵀ and of dPᵀ (64 queries each)
             uint32_t sr[64], dr[64];
             tmem_ld32(tmem + lane_base + L::S_COL + c0, sr);
@@ -346,7 +347,7 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             tmem_wait_ld();
             // P = exp2(S·scale·log2 e − LSE·log2 e), with the distance bias
             // −sb |i' − key| of query column j (i' = q0 + c0 + j + m − n) under BIAS
-            const float d1 = static_cast<float>(q0 + c0 + p.causal_off - key);
+            const float d1 = static_cast<float>(q0 + c0 + off - key);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 float lz[32];
@@ -361,7 +362,7 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             }
             if (need_mask) {
                 // this key is visible to the query columns j in [j_lo, j_hi) of the tile
-                const int q_first = key >= kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - p.causal_off : 0);
+                const int q_first = key >= kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - off : 0);
                 const int j_lo = q_first == INT32_MAX ? BM : max(q_first - q0, 0) - c0;
                 const int j_hi = min(p.n - q0, BM) - c0;
 #pragma unroll
@@ -578,6 +579,7 @@ struct LayoutPipe {
 // One work item: a 128-key tile of one (b, h) pair and the query tiles that see it.
 struct BwdItem {
     int bh, k0, kv_len, qb_lo, nt;   // nt = 0: no query sees these keys (zero gradients)
+    int off;                         // query row i sits at key position i + off
 };
 
 template <int MASK>
@@ -609,8 +611,9 @@ __device__ __forceinline__ BwdItem bwd_item(int u, int iu, const BwdParams& p)
         w.kv_len = len < 0 ? 0 : (len > p.m ? p.m : len);
     }
     w.qb_lo = 0;
+    w.off = causal_offset(MASK, p.causal_off, w.kv_len, p.n);
     if (mask_is_causal(MASK)) {
-        const int first_q = w.k0 - p.causal_off;     // first row that sees key k0
+        const int first_q = w.k0 - w.off;            // first row that sees key k0
         w.qb_lo = first_q <= 0 ? 0 : first_q / BM;
     }
     const int nqb = (p.n + BM - 1) / BM;
@@ -964,10 +967,10 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     mbar_arrive(bar(L::B_RDONE));    // the MMA warp may compute the next Sᵀ, dPᵀ
                     const uint32_t lse_s = sbase + L::LSE_OFF + (s * BM + c0) * 4;
                     const uint32_t dd_s = sbase + L::DD_OFF + (s * BM + c0) * 4;
-                    const float d1 = static_cast<float>(q0 + c0 + p.causal_off - key);
+                    const float d1 = static_cast<float>(q0 + c0 + w.off - key);
                     const bool need_mask =
                         __any_sync(0xffffffffu, key >= w.kv_len || q0 + c0 + 63 >= p.n ||
-                                                    (mask_is_causal(MASK) && key > q0 + c0 + p.causal_off));
+                                                    (mask_is_causal(MASK) && key > q0 + c0 + w.off));
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
                         float lz[32];
@@ -983,7 +986,7 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     }
                     if (need_mask) {
                         const int q_first =
-                            key >= w.kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - p.causal_off : 0);
+                            key >= w.kv_len ? INT32_MAX : (mask_is_causal(MASK) ? key - w.off : 0);
                         const int j_lo = q_first == INT32_MAX ? BM : max(q_first - q0, 0) - c0;
                         const int j_hi = min(p.n - q0, BM) - c0;
 #pragma unroll

@@ -108,7 +108,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         kv_len = len < 0 ? 0 : (len > p.m ? p.m : len);
     }
     int last = kv_len;                                   // one past the last visible key
-    if (mask_is_causal(p.mask)) last = min(last, max(0, p.n - 1 + p.causal_off + 1));
+    const int off = causal_offset(p.mask, p.causal_off, kv_len, p.n);   // row i sits at key position i + off
+    if (mask_is_causal(p.mask)) last = min(last, max(0, p.n - 1 + off + 1));
     const int j0 = split * p.split_len;
     const int j1 = min(j0 + p.split_len, last);
     const int ntiles = j1 > j0 ? (j1 - j0 + TILE_KEYS - 1) / TILE_KEYS : 0;
@@ -220,9 +221,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         float pr[NQ];
 #pragma unroll
         for (int i = 0; i < NQ; ++i) {
-            const bool vis = key < j1 && (!mask_is_causal(p.mask) || key <= i + p.causal_off);
+            const bool vis = key < j1 && (!mask_is_causal(p.mask) || key <= i + off);
             const float x =
-                vis ? fmaf(-sb, fabsf(static_cast<float>(i + p.causal_off - key)), sc[i] * sl2) : -INFINITY;
+                vis ? fmaf(-sb, fabsf(static_cast<float>(i + off - key)), sc[i] * sl2) : -INFINITY;
             float mx = x;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));

@@ -121,6 +121,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
 // One query tile of work: (b, h) pair, first query row, key tiles to visit.
 struct Unit {
     int bh, q0, kv_len, nkv;
+    int off;   // query row i sits at key position i + off (the causal masks' diagonal)
 };
 
 // Work units are numbered head-major so that concurrently running units share
@@ -156,9 +157,10 @@ __device__ __forceinline__ Unit tile_of(int u, int i, const FwdParams& p)
         w.kv_len = len < 0 ? 0 : (len > p.m ? p.m : len);
     }
     w.nkv = (w.kv_len + BN - 1) / BN;
+    w.off = causal_offset(MASK, p.causal_off, w.kv_len, p.n);
     if (mask_is_causal(MASK)) {
         // the last key visible to the tile's last row; none if it is negative
-        const int last = min(w.q0 + BM - 1, p.n - 1) + p.causal_off;
+        const int last = min(w.q0 + BM - 1, p.n - 1) + w.off;
         w.nkv = last < 0 ? 0 : min(last / BN + 1, w.nkv);
     }
     return w;
@@ -436,7 +438,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (TilePos t = first_tile; ok && t.u < p.num_units; advance<MASK>(t, u_step, p)) {
             const Unit w = tile_of<MASK>(t.u, t.ti, p);
             const int qrow = w.q0 + r;
-            const int qlim = qrow + p.causal_off;   // the row's key position: last key it sees under the causal mask
+            const int qlim = qrow + w.off;   // the row's key position: last key it sees under the causal mask
             // distance-bias slope of the head, log2 domain
             const float sb = BIAS ? __ldg(p.slopes + w.bh % p.H) * LOG2E : 0.f;
             float m_ref = -INFINITY;

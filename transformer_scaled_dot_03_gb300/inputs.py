@@ -129,7 +129,12 @@ WORKLOADS.update({
     "decode_long_context": Workload("decode_long_context", 2, 16, 1, 32768, 128, 128, MASK_NONE, seed=9,
                                     path="decode"),
 })
-DECODE_ORDER = ["decode_kv_cache", "decode_long_context"]
+# A speculative-decoding check: 4 draft tokens per sequence verified against a
+# cache of 8192 slots filled to [4096, 8192] positions (the causal mask inside each
+# entry's filled cache), 64 sequences x 16 heads, d 128.
+WORKLOADS["spec_decode_cache"] = Workload("spec_decode_cache", 64, 16, 4, 8192, 128, 128, MASK_CAUSAL_CACHE,
+                                          seed=12, len_lo=4096, len_hi=8192, path="decode")
+DECODE_ORDER = ["decode_kv_cache", "decode_long_context", "spec_decode_cache"]
 
 # The linear distance bias ("第2章：完整的 Transformer 架构" §5.3) on the big-decoder
 # and the long-context causal self-attention.
