@@ -237,7 +237,7 @@ int attn_bwd_alibi(const void* Q, const void* K, const void* V, const void* O, c
  * system's rate without a merge.
  *   n            1..8 query rows per (b, h); 0 is a no-op; more is
  *                ATTN_ERR_UNSUPPORTED (use attn_fwd).
- *   d_k, d_v     equal, 64 or 128.
+ *   d_k, d_v     each 64 or 128 (d_k != d_v allowed).
  *   key_lengths  for the key-padding masks: the valid cache length per batch
  *                entry (as in attn_fwd).
  *   workspace    device scratch for the per-chunk partial results, owned by the

@@ -80,6 +80,21 @@ def test_decode_split_extremes(B, H, m):
     check(x, f"B={B} H={H} m={m}")
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64)])
+@pytest.mark.parametrize("mask,n,m", [("none", 1, 4097), ("causal", 8, 1000), ("key_padding", 3, 2000)])
+def test_decode_mixed_head_dims(dk, dv, mask, n, m):
+    """Value heads of another width than the key heads (one and several key chunks)."""
+    lens = [m, m // 3, 1] if mask in inputs.LENGTH_MASKS else None
+    x = inputs.make_inputs(3 if lens else 2, 4, n, m, dk, dv, mask, seed=7000 + dk + n + m, key_lengths=lens)
+    check(x, f"decode {mask} n={n} m={m} d_k={dk} d_v={dv}")
+
+
+def test_decode_mixed_head_dims_many_heads():
+    """Enough (b, h) pairs for the tensor-core path, d_k != d_v."""
+    x = inputs.make_inputs(64, 16, 2, 300, 64, 128, "none", seed=7100)
+    check(x, "decode many heads d_k=64 d_v=128")
+
+
 def test_decode_matches_attn_fwd():
     x = inputs.make_inputs(4, 8, 4, 2500, 64, 64, "key_padding", seed=9400, len_lo=1, len_hi=2500)
     Od, Ld = run_decode(x)

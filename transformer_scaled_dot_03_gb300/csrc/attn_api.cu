@@ -683,13 +683,13 @@ int decode_rows(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 
 extern "C" size_t attn_decode_workspace_size(int B, int H, int n, int m, int d_k, int d_v)
 {
-    (void)d_v;
-    if (B <= 0 || H <= 0 || n <= 0 || m <= 0 || d_k <= 0) return 0;
+    (void)d_k;
+    if (B <= 0 || H <= 0 || n <= 0 || m <= 0 || d_v <= 0) return 0;
     const int64_t bh = static_cast<int64_t>(B) * H;
     const int64_t cap = decode_split_cap(bh, m);
     if (cap == 1) return 0;
     const size_t rows = static_cast<size_t>(bh) * cap * n;
-    return round_up(rows * d_k * 4, kWsAlign) + round_up(rows * 2 * 4, kWsAlign);
+    return round_up(rows * d_v * 4, kWsAlign) + round_up(rows * 2 * 4, kWsAlign);
 }
 
 namespace {
@@ -702,7 +702,7 @@ int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n
     if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_CACHE) return ATTN_ERR_INVALID_ARG;
     if (attn::mask_has_lengths(mask_kind) && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_ok(d_k) || d_v != d_k || n > kDecodeMaxRows) return ATTN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(d_k) || !head_dim_ok(d_v) || n > kDecodeMaxRows) return ATTN_ERR_UNSUPPORTED;
     if (m > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || n == 0) return ATTN_OK;
     const int64_t bh = static_cast<int64_t>(B) * H;
@@ -719,8 +719,8 @@ int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n
     int num_sms = 0;
     int rc0 = sm_count(&num_sms);
     if (rc0 != ATTN_OK) return rc0;
-    const int64_t slots = static_cast<int64_t>(num_sms) * (d_k == 64 ? 2 : 1);
-    if (bh >= kDecodeTileWaves * slots) {
+    const int64_t slots = static_cast<int64_t>(num_sms) * (d_k == 64 && d_v == 64 ? 2 : 1);
+    if (bh >= kDecodeTileWaves * slots && (slopes == nullptr || d_k == d_v)) {
         // Enough (b, h) pairs to fill every SM several times over: the tensor-core
         // forward kernel streams each pair's K and V once at the memory system's
         // rate (its 128-row query tile is mostly padding, which the tensor cores
@@ -763,11 +763,11 @@ int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n
     // partials laid out for the cap's chunk count; the launch uses num_splits <= cap of them
     const size_t prow = static_cast<size_t>(bh) * decode_split_cap(bh, m) * n;
     p.part_o = num_splits > 1 ? reinterpret_cast<float*>(wsb) : nullptr;
-    p.part_ml = num_splits > 1 ? reinterpret_cast<float*>(wsb + round_up(prow * d_k * 4, kWsAlign)) : nullptr;
+    p.part_ml = num_splits > 1 ? reinterpret_cast<float*>(wsb + round_up(prow * d_v * 4, kWsAlign)) : nullptr;
     p.slopes = slopes;
     p.status = status;
     p.watchdog_ns = g_watchdog_ns;
-    cudaError_t e = attn::launch_decode(d_k, decode_rows(n), tmK, tmV, p, st);
+    cudaError_t e = attn::launch_decode(d_k, d_v, decode_rows(n), tmK, tmV, p, st);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("decode kernel launch", e);
 }
 

@@ -116,7 +116,7 @@ cudaError_t launch_bwd_alibi(int d, int mask, const BwdMaps& maps, const BwdPara
 
 // Few-row forward (attn_kernel_decode.cuh): one CTA per (b, h, key chunk).
 struct DecodeParams {
-    const uint16_t* Q;            // bf16 [B,H,n,d]
+    const uint16_t* Q;            // bf16 [B,H,n,d_k]
     int B, H, n, m;
     int causal_off;               // m - n
     int mask;
@@ -124,9 +124,9 @@ struct DecodeParams {
     float scale_log2;             // scale * log2(e)
     int split_len;                // keys per chunk (multiple of 128)
     int num_splits;               // chunks per (b, h)
-    uint16_t* O;                  // bf16 [B,H,n,d]
+    uint16_t* O;                  // bf16 [B,H,n,d_v]
     float* LSE;                   // fp32 [B,H,n] or null
-    float* part_o;                // fp32 [B*H, num_splits, n, d] (num_splits > 1)
+    float* part_o;                // fp32 [B*H, num_splits, n, d_v] (num_splits > 1)
     float* part_ml;               // fp32 [B*H, num_splits, n, 2]: max (log2 domain), sum
     const float* slopes;          // fp32 [H]: distance-bias slope per head, or null (no bias)
     uint32_t* status;
@@ -134,8 +134,8 @@ struct DecodeParams {
 };
 
 // rows: the kernel variant handles n <= rows (1, 2, 4 or 8).
-cudaError_t launch_decode(int d, int rows, const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p,
-                          cudaStream_t stream);
+cudaError_t launch_decode(int d_k, int d_v, int rows, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          const DecodeParams& p, cudaStream_t stream);
 
 // Projections around the attention (attn_kernel_proj.cuh): Y = A Wᵀ (+ bias).
 struct ProjParams {

@@ -44,19 +44,23 @@ constexpr int NQ_MAX = 8;
 constexpr float LN2 = 0.693147180559945309f;
 constexpr float LOG2E = 1.44269504088896341f;
 
-template <int D>
+// DK: query/key head dim, DV: value head dim.
+template <int DK, int DV>
 struct Layout {
-    static constexpr int CH = D / 64;
-    static constexpr int TILE = CH * CHUNK_BYTES;          // 128 keys x D
-    static constexpr int STAGES = D == 64 ? 3 : 2;
+    static constexpr int CHK = DK / 64;
+    static constexpr int CHV = DV / 64;
+    static constexpr int TILE_K = CHK * CHUNK_BYTES;        // 128 keys x DK
+    static constexpr int TILE_V = CHV * CHUNK_BYTES;        // 128 keys x DV
+    static constexpr bool SMALL = DK == 64 && DV == 64;
+    static constexpr int STAGES = SMALL ? 3 : 2;
     static constexpr int NUM_THREADS = 160;
     static constexpr int WARP_TMA = 4;
-    static constexpr int CTAS_PER_SM = D == 64 ? 2 : 1;
+    static constexpr int CTAS_PER_SM = SMALL ? 2 : 1;
     static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + STAGES * TILE;
-    static constexpr int Q_OFF = V_OFF + STAGES * TILE;     // fp32 [NQ_MAX][D]
-    static constexpr int RED_OFF = Q_OFF + NQ_MAX * D * 4;  // per warp: m, l [NQ_MAX] then O [NQ_MAX][D]
-    static constexpr int RED_WARP = (2 * NQ_MAX + NQ_MAX * D) * 4;
+    static constexpr int V_OFF = K_OFF + STAGES * TILE_K;
+    static constexpr int Q_OFF = V_OFF + STAGES * TILE_V;    // fp32 [NQ_MAX][DK]
+    static constexpr int RED_OFF = Q_OFF + NQ_MAX * DK * 4;  // per warp: m, l [NQ_MAX] then O [NQ_MAX][DV]
+    static constexpr int RED_WARP = (2 * NQ_MAX + NQ_MAX * DV) * 4;
     static constexpr int BAR_OFF = RED_OFF + 4 * RED_WARP;
     static constexpr int B_FULL = 0;
     static constexpr int B_EMPTY = STAGES;
@@ -71,19 +75,18 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 
 // Byte offset of element (row, col) in a 128-row tile stored as 64-column chunks
 // with the TMA 128-byte swizzle (16-byte pieces permuted by row % 8).
-template <int D>
 __device__ __forceinline__ uint32_t tile_off(int row, int col)
 {
     return static_cast<uint32_t>((col / 64) * CHUNK_BYTES + row * 128 +
                                  ((((col % 64) / 8) ^ (row & 7)) << 4) + (col % 8) * 2);
 }
 
-template <int D, int NQ>
-__global__ void __launch_bounds__(Layout<D>::NUM_THREADS, Layout<D>::CTAS_PER_SM)
+template <int DK, int DV, int NQ>
+__global__ void __launch_bounds__(Layout<DK, DV>::NUM_THREADS, Layout<DK, DV>::CTAS_PER_SM)
 attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const DecodeParams p)
 {
-    using L = Layout<D>;
+    using L = Layout<DK, DV>;
     griddep_wait();   // the previous grid's writes (Q, the cache, the lengths) are visible
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -123,14 +126,14 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
         fence_mbar_init();
     }
     // queries as fp32 (rows >= n are zero)
-    for (int e = threadIdx.x; e < NQ * D; e += blockDim.x) {
-        const int i = e / D, c = e % D;
+    for (int e = threadIdx.x; e < NQ * DK; e += blockDim.x) {
+        const int i = e / DK, c = e % DK;
         float v = 0.f;
         if (i < p.n) {
-            const uint16_t b = p.Q[(static_cast<int64_t>(bh) * p.n + i) * D + c];
+            const uint16_t b = p.Q[(static_cast<int64_t>(bh) * p.n + i) * DK + c];
             v = __uint_as_float(static_cast<uint32_t>(b) << 16);
         }
-        sq[i * D + c] = v;
+        sq[i * DK + c] = v;
     }
     __syncthreads();
 
@@ -146,13 +149,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                                p.status, STATUS_TMA_WAIT, limit))
                     break;
                 const int key0 = j0 + t * TILE_KEYS;
-                mbar_arrive_expect_tx(bar(L::B_FULL + s), 2 * L::TILE);
-                for (int c = 0; c < L::CH; ++c) {
-                    tma_load_3d(sbase + L::K_OFF + s * L::TILE + c * CHUNK_BYTES, &tmK, bar(L::B_FULL + s), c * 64,
+                mbar_arrive_expect_tx(bar(L::B_FULL + s), L::TILE_K + L::TILE_V);
+                for (int c = 0; c < L::CHK; ++c)
+                    tma_load_3d(sbase + L::K_OFF + s * L::TILE_K + c * CHUNK_BYTES, &tmK, bar(L::B_FULL + s), c * 64,
                                 key0, bh);
-                    tma_load_3d(sbase + L::V_OFF + s * L::TILE + c * CHUNK_BYTES, &tmV, bar(L::B_FULL + s), c * 64,
+                for (int c = 0; c < L::CHV; ++c)
+                    tma_load_3d(sbase + L::V_OFF + s * L::TILE_V + c * CHUNK_BYTES, &tmV, bar(L::B_FULL + s), c * 64,
                                 key0, bh);
-                }
                 ++issued;
             }
             // land every copy still in flight (only possible after an abort)
@@ -168,7 +171,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
 
     // ================================================== consumers (warps 0-3)
-    constexpr int CPL = D / 32;            // output columns per lane
+    constexpr int CPL = DV / 32;           // output columns per lane
     float m_run[NQ], l_run[NQ], o[NQ][CPL];
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
@@ -188,8 +191,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
                        STATUS_SOFTMAX_WAIT, limit);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
-        const uint8_t* kt = smem + L::K_OFF + s * L::TILE;
-        const uint8_t* vt = smem + L::V_OFF + s * L::TILE;
+        const uint8_t* kt = smem + L::K_OFF + s * L::TILE_K;
+        const uint8_t* vt = smem + L::V_OFF + s * L::TILE_V;
         const int key = j0 + t * TILE_KEYS + row;
 
         // scores of this lane's key against every row
@@ -197,14 +200,14 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
 #pragma unroll
         for (int i = 0; i < NQ; ++i) sc[i] = 0.f;
 #pragma unroll 4
-        for (int c8 = 0; c8 < D / 8; ++c8) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(kt + tile_off<D>(row, 8 * c8));
+        for (int c8 = 0; c8 < DK / 8; ++c8) {
+            const uint4 kv = *reinterpret_cast<const uint4*>(kt + tile_off(row, 8 * c8));
             const float k[8] = {bf16_lo(kv.x), bf16_hi(kv.x), bf16_lo(kv.y), bf16_hi(kv.y),
                                 bf16_lo(kv.z), bf16_hi(kv.z), bf16_lo(kv.w), bf16_hi(kv.w)};
 #pragma unroll
             for (int i = 0; i < NQ; ++i) {
-                const float4 qa = *reinterpret_cast<const float4*>(sq + i * D + 8 * c8);
-                const float4 qb = *reinterpret_cast<const float4*>(sq + i * D + 8 * c8 + 4);
+                const float4 qa = *reinterpret_cast<const float4*>(sq + i * DK + 8 * c8);
+                const float4 qb = *reinterpret_cast<const float4*>(sq + i * DK + 8 * c8 + 4);
                 float a = sc[i];
                 a = fmaf(qa.x, k[0], a);
                 a = fmaf(qa.y, k[1], a);
@@ -242,13 +245,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const int vrow = 32 * warp + jj;
             float v[CPL];
             if (CPL == 4) {
-                const uint2 vv = *reinterpret_cast<const uint2*>(vt + tile_off<D>(vrow, 4 * lane));
+                const uint2 vv = *reinterpret_cast<const uint2*>(vt + tile_off(vrow, 4 * lane));
                 v[0] = bf16_lo(vv.x);
                 v[1] = bf16_hi(vv.x);
                 v[2] = bf16_lo(vv.y);
                 v[3] = bf16_hi(vv.y);
             } else {
-                const uint32_t vv = *reinterpret_cast<const uint32_t*>(vt + tile_off<D>(vrow, 2 * lane));
+                const uint32_t vv = *reinterpret_cast<const uint32_t*>(vt + tile_off(vrow, 2 * lane));
                 v[0] = bf16_lo(vv);
                 v[1] = bf16_hi(vv);
             }
@@ -275,13 +278,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             red[NQ_MAX + i] = l;
         }
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) red[2 * NQ_MAX + i * D + CPL * lane + c] = o[i][c];
+        for (int c = 0; c < CPL; ++c) red[2 * NQ_MAX + i * DV + CPL * lane + c] = o[i][c];
     }
     // the producer warp has returned: synchronise the four consumer warps only
     asm volatile("bar.sync 1, 128;" ::: "memory");
     const int rows = min(p.n, NQ);
-    for (int e = threadIdx.x; e < rows * D; e += 128) {
-        const int i = e / D, c = e % D;
+    for (int e = threadIdx.x; e < rows * DV; e += 128) {
+        const int i = e / DV, c = e % DV;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < 4; ++w) M = fmaxf(M, sred[w * (L::RED_WARP / 4) + i]);
@@ -292,17 +295,17 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             const float* rw = sred + w * (L::RED_WARP / 4);
             const float f = ex2_approx(rw[i] - M_use);
             Lsum = fmaf(rw[NQ_MAX + i], f, Lsum);
-            Oc = fmaf(rw[2 * NQ_MAX + i * D + c], f, Oc);
+            Oc = fmaf(rw[2 * NQ_MAX + i * DV + c], f, Oc);
         }
         const int64_t orow = static_cast<int64_t>(bh) * p.n + i;
         if (p.num_splits == 1) {
             const float out = Lsum > 0.f ? Oc / Lsum : 0.f;
             const uint32_t pk = pack_bf16x2(out, 0.f);
-            p.O[orow * D + c] = static_cast<uint16_t>(pk & 0xFFFFu);
+            p.O[orow * DV + c] = static_cast<uint16_t>(pk & 0xFFFFu);
             if (c == 0 && p.LSE != nullptr) p.LSE[orow] = Lsum > 0.f ? (M + __log2f(Lsum)) * LN2 : -INFINITY;
         } else {
             const int64_t prow = (static_cast<int64_t>(bh) * p.num_splits + split) * p.n + i;
-            p.part_o[prow * D + c] = Oc;
+            p.part_o[prow * DV + c] = Oc;
             if (c == 0) {
                 p.part_ml[2 * prow] = M;
                 p.part_ml[2 * prow + 1] = Lsum;
@@ -335,11 +338,11 @@ attn_decode_combine_kernel(const DecodeParams p)
     if (c == 0 && p.LSE != nullptr) p.LSE[r] = Lsum > 0.f ? (M + __log2f(Lsum)) * LN2 : -INFINITY;
 }
 
-template <int D, int NQ>
+template <int DK, int DV, int NQ>
 cudaError_t launch(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p, cudaStream_t stream)
 {
-    using L = Layout<D>;
-    auto kern = attn_decode_kernel<D, NQ>;
+    using L = Layout<DK, DV>;
+    auto kern = attn_decode_kernel<DK, DV, NQ>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -353,8 +356,8 @@ cudaError_t launch(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeP
     const int64_t grid = static_cast<int64_t>(p.B) * p.H * p.num_splits;
     e = launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(L::NUM_THREADS), L::BYTES, stream, tmK, tmV, p);
     if (e != cudaSuccess || p.num_splits == 1) return e;
-    return launch_pdl(attn_decode_combine_kernel<D>, dim3(static_cast<unsigned>(static_cast<int64_t>(p.B) * p.H * p.n)),
-                      dim3(D), 0, stream, p);
+    return launch_pdl(attn_decode_combine_kernel<DV>, dim3(static_cast<unsigned>(static_cast<int64_t>(p.B) * p.H * p.n)),
+                      dim3(DV), 0, stream, p);
 }
 
 }  // namespace dec
