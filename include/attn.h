@@ -189,7 +189,7 @@ int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int B, int H, 
  *   O, LSE       the forward's outputs for these inputs (bf16 [B,H,n,d_v],
  *                fp32 [B,H,n]); LSE may not be NULL.
  *   dO           bf16 [B,H,n,d_v], the gradient of the loss with respect to O.
- *   B..scale     as in attn_fwd; supported: d_k == d_v in {64, 128}.
+ *   B..scale     as in attn_fwd; d_k, d_v each 64 or 128 (d_k != d_v allowed).
  *   dQ, dK, dV   bf16 outputs [B,H,n,d_k], [B,H,m,d_k], [B,H,m,d_v]. Keys that
  *                no query sees (masked for every row) get exactly 0. n = 0
  *                writes dK = dV = 0; m = 0 writes dQ = 0.

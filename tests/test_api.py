@@ -118,7 +118,7 @@ def call_bwd(B=1, H=1, n=4, m=4, dk=64, dv=64, mask=0, lens=None, dQ=P2, dK=P2, 
     (dict(mask=4), attn.ATTN_ERR_INVALID_ARG),          # the cache mask without key lengths
     (dict(mask=2, lens=None), attn.ATTN_ERR_INVALID_ARG),
     (dict(mask=3, lens=None), attn.ATTN_ERR_INVALID_ARG),
-    (dict(dk=64, dv=128), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dk=64, dv=96), attn.ATTN_ERR_UNSUPPORTED),
     (dict(dk=96, dv=96), attn.ATTN_ERR_UNSUPPORTED),
     (dict(dQ=None), attn.ATTN_ERR_INVALID_ARG),
     (dict(dK=None), attn.ATTN_ERR_INVALID_ARG),

@@ -100,6 +100,22 @@ def test_bwd_matches_oracle(d, mask, n, m, lens):
     check_bwd(x, dO, f"{mask} n={n} m={m} d={d}")
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64)])
+@pytest.mark.parametrize("mask,n,m,lens", [
+    ("none", 200, 200, None),
+    ("causal", 256, 256, None),
+    ("causal", 130, 300, None),
+    ("key_padding", 150, 260, [260, 1, 0, 129]),
+    ("causal_key_padding", 100, 333, [333, 250, 234, 1]),
+])
+def test_bwd_mixed_head_dims(dk, dv, mask, n, m, lens):
+    """Value heads of another width than the query/key heads."""
+    B = len(lens) if lens else 2
+    x = inputs.make_inputs(B, 2, n, m, dk, dv, mask, seed=8500 + n + m + dk, key_lengths=lens)
+    dO = inputs.make_grad_output(B, 2, n, dv, seed=8501 + n + m + dk)
+    check_bwd(x, dO, f"{mask} n={n} m={m} d_k={dk} d_v={dv}")
+
+
 def test_bwd_big_decoder_small_batch():
     """Big-decoder sizes (n = m = 1024, d 64, causal) on 2 x 4 heads, every element."""
     x, dO = case(2, 4, 1024, 1024, 64, "causal", seed=8100)

@@ -521,7 +521,7 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
     if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_CACHE) return ATTN_ERR_INVALID_ARG;
     if (attn::mask_has_lengths(mask_kind) && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_ok(d_k) || d_v != d_k) return ATTN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(d_k) || !head_dim_ok(d_v) || (slopes != nullptr && d_v != d_k)) return ATTN_ERR_UNSUPPORTED;
     if (n > kMaxSeq || m > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0) return ATTN_OK;
     const int64_t bh = static_cast<int64_t>(B) * H;
@@ -601,6 +601,8 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
     if (e != cudaSuccess) return fail_cuda("backward preparation kernel launch", e);
     if (slopes != nullptr)
         e = attn::launch_bwd_alibi(d_k, mask_kind, maps, p, st);
+    else if (d_k != d_v)
+        e = attn::launch_bwd_dmix(d_k, d_v, mask_kind, maps, p, st);
     else
         e = d_k == 64 ? attn::launch_bwd_d64(mask_kind, maps, p, st) : attn::launch_bwd_d128(mask_kind, maps, p, st);
     if (e != cudaSuccess) return fail_cuda("backward kernel launch", e);

@@ -9,11 +9,11 @@ template <int D>
 static cudaError_t launch_bias(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream)
 {
     switch (mask) {
-    case MASK_NONE: return bwd::launch<D, MASK_NONE, true>(maps, p, stream);
-    case MASK_CAUSAL: return bwd::launch<D, MASK_CAUSAL, true>(maps, p, stream);
-    case MASK_KEY_PADDING: return bwd::launch<D, MASK_KEY_PADDING, true>(maps, p, stream);
-    case MASK_CAUSAL_KEY_PADDING: return bwd::launch<D, MASK_CAUSAL_KEY_PADDING, true>(maps, p, stream);
-    case MASK_CAUSAL_CACHE: return bwd::launch<D, MASK_CAUSAL_CACHE, true>(maps, p, stream);
+    case MASK_NONE: return bwd::launch<D, D, MASK_NONE, true>(maps, p, stream);
+    case MASK_CAUSAL: return bwd::launch<D, D, MASK_CAUSAL, true>(maps, p, stream);
+    case MASK_KEY_PADDING: return bwd::launch<D, D, MASK_KEY_PADDING, true>(maps, p, stream);
+    case MASK_CAUSAL_KEY_PADDING: return bwd::launch<D, D, MASK_CAUSAL_KEY_PADDING, true>(maps, p, stream);
+    case MASK_CAUSAL_CACHE: return bwd::launch<D, D, MASK_CAUSAL_CACHE, true>(maps, p, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -6,11 +6,11 @@ namespace attn {
 cudaError_t launch_bwd_d128(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream)
 {
     switch (mask) {
-    case MASK_NONE: return bwd::launch<128, MASK_NONE>(maps, p, stream);
-    case MASK_CAUSAL: return bwd::launch<128, MASK_CAUSAL>(maps, p, stream);
-    case MASK_KEY_PADDING: return bwd::launch<128, MASK_KEY_PADDING>(maps, p, stream);
-    case MASK_CAUSAL_KEY_PADDING: return bwd::launch<128, MASK_CAUSAL_KEY_PADDING>(maps, p, stream);
-    case MASK_CAUSAL_CACHE: return bwd::launch<128, MASK_CAUSAL_CACHE>(maps, p, stream);
+    case MASK_NONE: return bwd::launch<128, 128, MASK_NONE>(maps, p, stream);
+    case MASK_CAUSAL: return bwd::launch<128, 128, MASK_CAUSAL>(maps, p, stream);
+    case MASK_KEY_PADDING: return bwd::launch<128, 128, MASK_KEY_PADDING>(maps, p, stream);
+    case MASK_CAUSAL_KEY_PADDING: return bwd::launch<128, 128, MASK_CAUSAL_KEY_PADDING>(maps, p, stream);
+    case MASK_CAUSAL_CACHE: return bwd::launch<128, 128, MASK_CAUSAL_CACHE>(maps, p, stream);
     default: return cudaErrorInvalidValue;
     }
 }

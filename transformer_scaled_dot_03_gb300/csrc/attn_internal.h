@@ -111,6 +111,8 @@ struct BwdMaps {
 
 cudaError_t launch_bwd_d64(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_d128(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+// Backward for d_k != d_v (64 and 128 either way round).
+cudaError_t launch_bwd_dmix(int d_k, int d_v, int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 // Backward with the linear distance bias (p.slopes), d_k = d_v = d in {64, 128}.
 cudaError_t launch_bwd_alibi(int d, int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 

@@ -51,20 +51,23 @@ constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // keys per CTA
 constexpr int CHUNK_BYTES = 128 * 64 * 2;
 
-template <int D>
+// DK: query/key head dim, DV: value head dim.
+template <int DK, int DV>
 struct Layout {
-    static constexpr int CH = D / 64;
-    static constexpr int TILE = CH * CHUNK_BYTES;        // a 128 x D bf16 tile
+    static constexpr int CHK = DK / 64;
+    static constexpr int CHV = DV / 64;
+    static constexpr int TILE_K = CHK * CHUNK_BYTES;     // a 128 x DK bf16 tile (K, Q)
+    static constexpr int TILE_V = CHV * CHUNK_BYTES;     // a 128 x DV bf16 tile (V, dO)
     static constexpr int NUM_THREADS = 320;
     static constexpr int COMPUTE_THREADS = 256;
     static constexpr int WARP_TMA = 8;
     static constexpr int WARP_MMA = 9;
-    static constexpr int QS = D == 64 ? 2 : 1;             // Q/dO/LSE/D ring depth
+    static constexpr int QS = DK == 64 && DV == 64 ? 2 : 1;   // Q/dO/LSE/D ring depth
     static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + TILE;
-    static constexpr int Q_OFF = V_OFF + TILE;
-    static constexpr int DO_OFF = Q_OFF + QS * TILE;
-    static constexpr int DS_OFF = DO_OFF + QS * TILE;      // dS (bf16, MN-major) / staging, 32 KB
+    static constexpr int V_OFF = K_OFF + TILE_K;
+    static constexpr int Q_OFF = V_OFF + TILE_V;
+    static constexpr int DO_OFF = Q_OFF + QS * TILE_K;
+    static constexpr int DS_OFF = DO_OFF + QS * TILE_V;    // dS (bf16, MN-major) / staging, 32 KB
     static constexpr int LSE_OFF = DS_OFF + 2 * CHUNK_BYTES;
     static constexpr int DD_OFF = LSE_OFF + QS * BM * 4;
     static constexpr int BAR_OFF = DD_OFF + QS * BM * 4;
@@ -85,10 +88,13 @@ struct Layout {
     static constexpr int BYTES = MISC_OFF + 16 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 0, DP_COL = 128, P_COL = 0, DS_COL = 128;
-    static constexpr uint32_t DV_COL = 256, DK_COL = 256 + D;
-    static constexpr bool DQ_OVER_S = D == 128;            // dQ halves reuse the upper Sᵀ/dPᵀ columns
-    __host__ __device__ static constexpr uint32_t dq_col(int h) { return DQ_OVER_S ? (h == 0 ? 64u : 192u) : 384u; }
-    static_assert(DK_COL + D <= TMEM_COLS, "tensor memory layout");
+    static constexpr uint32_t DV_COL = 256, DK_COL = 256 + DV;
+    static constexpr bool DQ_OVER_S = DK == 128;           // dQ halves reuse the upper Sᵀ/dPᵀ columns
+    __host__ __device__ static constexpr uint32_t dq_col(int h)
+    {
+        return DQ_OVER_S ? (h == 0 ? 64u : 192u) : DK_COL + DK;
+    }
+    static_assert(DK_COL + DK <= TMEM_COLS && (DQ_OVER_S || DK_COL + 2 * DK <= TMEM_COLS), "tensor memory layout");
     static_assert(BYTES <= 232448, "shared memory budget");
 };
 
@@ -101,11 +107,11 @@ __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, uint64_t li
     return true;
 }
 
-template <int D, int MASK, bool BIAS>
-__global__ void __launch_bounds__(Layout<D>::NUM_THREADS, 1)
+template <int DK, int DV, int MASK, bool BIAS>
+__global__ void __launch_bounds__(Layout<DK, DV>::NUM_THREADS, 1)
 attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 {
-    using L = Layout<D>;
+    using L = Layout<DK, DV>;
     griddep_wait();   // the preparation kernel's D, LSE rows and zeroed dQ accumulator are visible
     const int kb = static_cast<int>(blockIdx.x) % p.num_kblocks;
     const int bh = static_cast<int>(blockIdx.x) / p.num_kblocks;
@@ -118,13 +124,11 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     if (k0 >= kv_len) {
         // no query sees these keys: their gradients are zero
         const int rows = min(BN, p.m - k0);
-        const int64_t base = (static_cast<int64_t>(bh) * p.m + k0) * D;
-        uint4* gk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dK) + base);
-        uint4* gv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dV) + base);
-        for (int i = threadIdx.x; i < rows * D / 8; i += blockDim.x) {
-            gk[i] = make_uint4(0u, 0u, 0u, 0u);
-            gv[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
+        const int64_t base = static_cast<int64_t>(bh) * p.m + k0;
+        uint4* gk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dK) + base * DK);
+        uint4* gv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dV) + base * DV);
+        for (int i = threadIdx.x; i < rows * DK / 8; i += blockDim.x) gk[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = threadIdx.x; i < rows * DV / 8; i += blockDim.x) gv[i] = make_uint4(0u, 0u, 0u, 0u);
         return;
     }
     // query tiles that can see this key tile
@@ -194,11 +198,11 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     if (warp >= L::WARP_TMA) {
         if (warp == L::WARP_TMA && lane == 0) {
             // ================================================== TMA producer
-            mbar_arrive_expect_tx(bar(L::B_KVFULL), 2 * L::TILE);
-            for (int c = 0; c < L::CH; ++c) {
+            mbar_arrive_expect_tx(bar(L::B_KVFULL), L::TILE_K + L::TILE_V);
+            for (int c = 0; c < L::CHK; ++c)
                 tma_load_3d(sK + c * CHUNK_BYTES, &maps.k, bar(L::B_KVFULL), c * 64, k0, bh);
+            for (int c = 0; c < L::CHV; ++c)
                 tma_load_3d(sV + c * CHUNK_BYTES, &maps.v, bar(L::B_KVFULL), c * 64, k0, bh);
-            }
             int issued = 0;
             for (int t = 0; t < nt; ++t) {
                 const int s = t % L::QS;
@@ -207,12 +211,12 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                                p.status, STATUS_TMA_WAIT, limit))
                     break;
                 const int q0 = (qb_lo + t) * BM;
-                mbar_arrive_expect_tx(bar(L::B_QFULL + s), 2 * L::TILE + 2 * BM * 4);
-                for (int c = 0; c < L::CH; ++c) {
-                    tma_load_3d(sQ + s * L::TILE + c * CHUNK_BYTES, &maps.q, bar(L::B_QFULL + s), c * 64, q0, bh);
-                    tma_load_3d(sdO + s * L::TILE + c * CHUNK_BYTES, &maps.dout, bar(L::B_QFULL + s), c * 64, q0,
+                mbar_arrive_expect_tx(bar(L::B_QFULL + s), L::TILE_K + L::TILE_V + 2 * BM * 4);
+                for (int c = 0; c < L::CHK; ++c)
+                    tma_load_3d(sQ + s * L::TILE_K + c * CHUNK_BYTES, &maps.q, bar(L::B_QFULL + s), c * 64, q0, bh);
+                for (int c = 0; c < L::CHV; ++c)
+                    tma_load_3d(sdO + s * L::TILE_V + c * CHUNK_BYTES, &maps.dout, bar(L::B_QFULL + s), c * 64, q0,
                                 bh);
-                }
                 const int64_t row0 = static_cast<int64_t>(bh) * p.n_pad + q0;
                 bulk_load(sbase + L::LSE_OFF + s * BM * 4, p.lse2 + row0, BM * 4, bar(L::B_QFULL + s));
                 bulk_load(sbase + L::DD_OFF + s * BM * 4, p.dd + row0, BM * 4, bar(L::B_QFULL + s));
@@ -225,7 +229,8 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         } else if (warp == L::WARP_MMA) {
             // ================================================== MMA issuer (whole warp, one elected lane)
             constexpr uint32_t ID_S = idesc_bf16_f32(BN, BM, false, false);   // M = keys, N = queries
-            constexpr uint32_t ID_KV = idesc_bf16_f32(BN, D, false, true);    // M = keys, N = d
+            constexpr uint32_t ID_DV = idesc_bf16_f32(BN, DV, false, true);   // M = keys, N = d_v
+            constexpr uint32_t ID_DK = idesc_bf16_f32(BN, DK, false, true);   // M = keys, N = d_k
             constexpr uint32_t ID_DQ = idesc_bf16_f32(BM, 64, true, true);    // M = queries, N = 64
             const uint64_t dK_k = sdesc_sw128(sK, 16, 1024);
             const uint64_t dV_k = sdesc_sw128(sV, 16, 1024);
@@ -244,15 +249,15 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 if (ok && L::DQ_OVER_S && t > 0) ok = wait(L::B_DQFREE, parity ^ 1u);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t dQ_k = sdesc_sw128(sQ + s * L::TILE, 16, 1024);
-                const uint64_t dO_k = sdesc_sw128(sdO + s * L::TILE, 16, 1024);
+                const uint64_t dQ_k = sdesc_sw128(sQ + s * L::TILE_K, 16, 1024);
+                const uint64_t dO_k = sdesc_sw128(sdO + s * L::TILE_V, 16, 1024);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < DK / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>(((kk / 4) * CHUNK_BYTES + (kk % 4) * 32) >> 4);
                     mma_ss_warp(tmem + L::S_COL, dK_k + off, dQ_k + off, ID_S, kk > 0 ? 1u : 0u);
                 }
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < DV / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>(((kk / 4) * CHUNK_BYTES + (kk % 4) * 32) >> 4);
                     mma_ss_warp(tmem + L::DP_COL, dV_k + off, dO_k + off, ID_S, kk > 0 ? 1u : 0u);
                 }
@@ -261,22 +266,22 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 if (ok && !L::DQ_OVER_S && t > 0) ok = wait(L::B_DQFREE, parity ^ 1u);
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t dO_mn = sdesc_sw128(sdO + s * L::TILE, CHUNK_BYTES, 1024);
-                const uint64_t dQ_mn = sdesc_sw128(sQ + s * L::TILE, CHUNK_BYTES, 1024);
+                const uint64_t dO_mn = sdesc_sw128(sdO + s * L::TILE_V, CHUNK_BYTES, 1024);
+                const uint64_t dQ_mn = sdesc_sw128(sQ + s * L::TILE_K, CHUNK_BYTES, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
-                    mma_ts_warp(tmem + L::DV_COL, tmem + L::P_COL + kk * 8, dO_mn + off, ID_KV,
+                    mma_ts_warp(tmem + L::DV_COL, tmem + L::P_COL + kk * 8, dO_mn + off, ID_DV,
                                 (t > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
                 for (int kk = 0; kk < BM / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
-                    mma_ts_warp(tmem + L::DK_COL, tmem + L::DS_COL + kk * 8, dQ_mn + off, ID_KV,
+                    mma_ts_warp(tmem + L::DK_COL, tmem + L::DS_COL + kk * 8, dQ_mn + off, ID_DK,
                                 (t > 0 || kk > 0) ? 1u : 0u);
                 }
 #pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
+                for (int h = 0; h < DK / 64; ++h) {
                     const uint64_t dKh_mn = sdesc_sw128(sK + h * CHUNK_BYTES, CHUNK_BYTES, 1024);
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
@@ -421,12 +426,12 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             // d = 64: this warpgroup's 32 of the 64 dQ columns; d = 128: its 64 (two chunks
             // of 32, one after the other through this warp's staging rows)
 #pragma unroll 1
-            for (int k = 0; k < D / 64; ++k) {
-                const int col = D == 64 ? 32 * half : 64 * half + 32 * k;   // dQ column of the chunk
+            for (int k = 0; k < DK / 64; ++k) {
+                const int col = DK == 64 ? 32 * half : 64 * half + 32 * k;   // dQ column of the chunk
                 uint32_t a[32];
                 tmem_ld32(tmem + lane_base + L::dq_col(col / 64) + (col % 64), a);
                 tmem_wait_ld();
-                if (k == D / 64 - 1) {
+                if (k == DK / 64 - 1) {
                     tc_fence_before();
                     mbar_arrive(bar(L::B_DQFREE));
                 }
@@ -463,13 +468,14 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             for (int which = 0; which < 2; ++which) {
                 const uint32_t col = which == 0 ? L::DV_COL : L::DK_COL;
                 const float mul = which == 0 ? 1.f : p.scale;
+                const int Dw = which == 0 ? DV : DK;   // head dim of the gradient
                 wait_stores_read();
                 // both warpgroups' earlier stores have read the staging
                 ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
                 if (!ok) break;
 #pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc) {
-                    const int c = half * (D / 2) + 32 * cc;   // first column of this 32-column piece
+                for (int cc = 0; cc < Dw / 64; ++cc) {
+                    const int c = half * (Dw / 2) + 32 * cc;   // first column of this 32-column piece
                     uint32_t o[32];
                     tmem_ld32(tmem + lane_base + col + c, o);
                     tmem_wait_ld();
@@ -492,10 +498,10 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 // both halves of every staged row are written
                 ok = rendezvous(L::B_EPI, static_cast<uint32_t>(epi_phase++) & 1u);
                 if (!ok) break;
-                const bool storer = D == 64 ? half == 0 : true;
+                const bool storer = Dw == 64 ? half == 0 : true;
                 if (storer && lane == 0 && k0 + 32 * wq < p.m) {
                     const CUtensorMap* map = which == 0 ? &maps.dv : &maps.dk;
-                    const int c = D == 64 ? 0 : half;
+                    const int c = Dw == 64 ? 0 : half;
                     tma_store_3d(map, sdS + c * CHUNK_BYTES + wq * 32 * 128, c * 64, k0 + 32 * wq, bh);
                     bulk_commit_group();
                     store_pending = true;
@@ -1110,11 +1116,12 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     }
 }
 
-template <int D, int MASK, bool BIAS = false>
+template <int DK, int DV, int MASK, bool BIAS = false>
 cudaError_t launch(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream)
 {
-    using L = typename std::conditional<D == 64, LayoutPipe, Layout<D>>::type;
-    auto kern = D == 64 ? attn_bwd_pipe_kernel<MASK, BIAS> : attn_bwd_kernel<D, MASK, BIAS>;
+    constexpr bool PIPE = DK == 64 && DV == 64;
+    using L = typename std::conditional<PIPE, LayoutPipe, Layout<DK, DV>>::type;
+    auto kern = PIPE ? attn_bwd_pipe_kernel<MASK, BIAS> : attn_bwd_kernel<DK, DV, MASK, BIAS>;
     static bool configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1126,7 +1133,7 @@ cudaError_t launch(const BwdMaps& maps, const BwdParams& p, cudaStream_t stream)
         configured[dev] = true;
     }
     int64_t grid = static_cast<int64_t>(p.B) * p.H * p.num_kblocks;
-    if (D == 64) {
+    if (PIPE) {
         // persistent: one CTA per SM over units of one or two key tiles
         const int64_t units = static_cast<int64_t>(p.B) * p.H *
                               (mask_is_causal(MASK) ? (p.num_kblocks + 1) / 2 : p.num_kblocks);
