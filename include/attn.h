@@ -119,9 +119,9 @@ int attn_fwd(const void* Q, const void* K, const void* V, int B, int H, int n, i
  *   slopes       device fp32 [H], caller-owned, 4-byte aligned: the slope of
  *                every head in the units of the scaled scores (natural-log
  *                domain). Any finite values; 0 is no bias.
- *   other arguments as in attn_fwd; supported: d_k == d_v in {64, 128}.
- * Returns ATTN_OK or a negative attn_status_t (INVALID_ARG when slopes is NULL,
- * UNSUPPORTED when d_k != d_v); on error nothing is enqueued. Its decoding
+ *   other arguments as in attn_fwd (d_k, d_v each 64 or 128).
+ * Returns ATTN_OK or a negative attn_status_t (INVALID_ARG when slopes is NULL);
+ * on error nothing is enqueued. Its decoding
  * form is attn_decode_alibi, its backward attn_bwd_alibi.
  */
 int attn_fwd_alibi(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
@@ -235,8 +235,9 @@ int attn_bwd_alibi(const void* Q, const void* K, const void* V, const void* O, c
  * split over the keys and merges the chunks; with more pairs it runs the
  * tensor-core kernel of attn_fwd, which then streams K and V at the memory
  * system's rate without a merge.
- *   n            1..8 query rows per (b, h); 0 is a no-op; more is
- *                ATTN_ERR_UNSUPPORTED (use attn_fwd).
+ *   n            query rows per (b, h); 0 is a no-op. Up to 8 rows take the
+ *                split kernel described below; more always take the
+ *                tensor-core kernel of attn_fwd (no workspace).
  *   d_k, d_v     each 64 or 128 (d_k != d_v allowed).
  *   key_lengths  for the key-padding masks: the valid cache length per batch
  *                entry (as in attn_fwd).

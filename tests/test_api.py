@@ -150,7 +150,6 @@ def call_dec(B=1, H=1, n=1, m=4096, dk=64, dv=64, mask=0, lens=None, O=P2, ws=P,
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(n=9), attn.ATTN_ERR_UNSUPPORTED),
     (dict(dk=64, dv=96), attn.ATTN_ERR_UNSUPPORTED),
     (dict(dk=32, dv=32), attn.ATTN_ERR_UNSUPPORTED),
     (dict(mask=2, lens=None), attn.ATTN_ERR_INVALID_ARG),
@@ -172,6 +171,8 @@ def test_decode_workspace_size():
     # sized for the largest chunk count a launch may pick: min(ceil(m/256), ceil(2048/(B*H)))
     assert attn.decode_workspace_size(40, 16, 2, 4096, 128, 128) == 640 * 4 * 2 * 128 * 4 + 640 * 4 * 2 * 8
     assert attn.decode_workspace_size(0, 16, 1, 4096, 128, 128) == 0
+    # more than 8 rows run the tensor-core kernel: no workspace
+    assert attn.decode_workspace_size(1, 1, 9, 4096, 64, 64) == 0
     # the partial outputs have the value head dim
     assert attn.decode_workspace_size(1, 1, 1, 4096, 128, 64) == 16 * 64 * 4 + 256
     assert attn.decode_workspace_size(1, 1, 1, 4096, 64, 128) == 16 * 128 * 4 + 256

@@ -95,6 +95,13 @@ def test_decode_mixed_head_dims_many_heads():
     check(x, "decode many heads d_k=64 d_v=128")
 
 
+@pytest.mark.parametrize("n", [9, 16, 130])
+def test_decode_more_rows(n):
+    """More rows than the split kernel holds: the tensor-core kernel, few heads."""
+    x = inputs.make_inputs(2, 3, n, 1500, 128, 128, "causal", seed=7200 + n)
+    check(x, f"decode n={n}")
+
+
 def test_decode_matches_attn_fwd():
     x = inputs.make_inputs(4, 8, 4, 2500, 64, 64, "key_padding", seed=9400, len_lo=1, len_hi=2500)
     Od, Ld = run_decode(x)

@@ -116,6 +116,20 @@ def test_slope_range():
     check_full(x, slopes, "slope range")
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 128), (128, 64)])
+def test_mixed_head_dims(dk, dv):
+    x = inputs.make_inputs(3, 4, 200, 330, dk, dv, "causal_key_padding", seed=5600 + dk, key_lengths=[330, 200, 9])
+    check_full(x, inputs.alibi_slopes(4), f"bias d_k={dk} d_v={dv}")
+    # its decoding form and its backward
+    xd = inputs.make_inputs(2, 4, 3, 2000, dk, dv, "causal", seed=5601 + dk)
+    slopes = inputs.alibi_slopes(4)
+    O, L = run_decode(xd, slopes)
+    Or, Lr = oracle.attn_fwd(xd.Q, xd.K, xd.V, xd.mask, None, xd.scale, slopes=slopes)
+    A, _ = oracle.attn_fwd(xd.Q, xd.K, xd.V.abs(), xd.mask, None, xd.scale, slopes=slopes)
+    compare(O, L, Or, Lr, A, f"bias decode d_k={dk} d_v={dv}")
+    check_bwd(x, slopes, f"bias backward d_k={dk} d_v={dv}")
+
+
 def test_zero_slopes_match_attn_fwd():
     x = inputs.make_inputs(2, 3, 200, 200, 128, 128, "causal", seed=5200)
     O, L = run_gpu(x, torch.zeros(3))
@@ -136,8 +150,8 @@ def test_rejected_arguments():
     rc = lib.attn_fwd_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q.data_ptr()), 1, 2, 4, 4, 64, 64, 0, None, None,
                             ctypes.c_float(-1.0), vp(o.data_ptr()), None, stream)
     assert rc == attn.ATTN_ERR_INVALID_ARG
-    # d_k != d_v
-    rc = lib.attn_fwd_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q2.data_ptr()), 1, 2, 4, 4, 64, 128, 0, None,
+    # a head dim outside {64, 128}
+    rc = lib.attn_fwd_alibi(vp(q.data_ptr()), vp(q.data_ptr()), vp(q2.data_ptr()), 1, 2, 4, 4, 64, 96, 0, None,
                             vp(sl.data_ptr()), ctypes.c_float(-1.0), vp(o.data_ptr()), None, stream)
     assert rc == attn.ATTN_ERR_UNSUPPORTED
     # misaligned slopes

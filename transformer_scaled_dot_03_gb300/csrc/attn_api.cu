@@ -253,7 +253,7 @@ int launch_attention(const void* Q, const void* K, const void* V, int B, int H, 
     const int64_t ctas = bh * num_qblocks;
     cudaError_t e;
     if (slopes != nullptr)
-        e = attn::launch_fwd_alibi(d_k, mask_kind, maps, p, num_sms, st);
+        e = attn::launch_fwd_alibi(d_k, d_v, mask_kind, maps, p, num_sms, st);
     else if (d_k != d_v)
         e = attn::launch_fwd_dmix(d_k, d_v, mask_kind, maps, p, num_sms, st);
     else if (d_k == 64)
@@ -286,7 +286,6 @@ int attn_fwd_alibi(const void* Q, const void* K, const void* V, int B, int H, in
 {
     int rc = validate(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, O, LSE);
     if (rc != ATTN_OK || B == 0 || H == 0 || n == 0) return rc;
-    if (d_k != d_v) return ATTN_ERR_UNSUPPORTED;
     if (slopes == nullptr) return ATTN_ERR_INVALID_ARG;
     if (!aligned(slopes, 4)) return ATTN_ERR_MISALIGNED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -521,7 +520,7 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
     if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_CACHE) return ATTN_ERR_INVALID_ARG;
     if (attn::mask_has_lengths(mask_kind) && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_ok(d_k) || !head_dim_ok(d_v) || (slopes != nullptr && d_v != d_k)) return ATTN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(d_k) || !head_dim_ok(d_v)) return ATTN_ERR_UNSUPPORTED;
     if (n > kMaxSeq || m > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0) return ATTN_OK;
     const int64_t bh = static_cast<int64_t>(B) * H;
@@ -600,7 +599,7 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
                                      bh, n, ws.n_pad, d_v, lse2, dd, reinterpret_cast<float4*>(dq_acc), dq_vec);
     if (e != cudaSuccess) return fail_cuda("backward preparation kernel launch", e);
     if (slopes != nullptr)
-        e = attn::launch_bwd_alibi(d_k, mask_kind, maps, p, st);
+        e = attn::launch_bwd_alibi(d_k, d_v, mask_kind, maps, p, st);
     else if (d_k != d_v)
         e = attn::launch_bwd_dmix(d_k, d_v, mask_kind, maps, p, st);
     else
@@ -686,7 +685,7 @@ int decode_rows(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : n <= 4 ? 4 : 8; }
 extern "C" size_t attn_decode_workspace_size(int B, int H, int n, int m, int d_k, int d_v)
 {
     (void)d_k;
-    if (B <= 0 || H <= 0 || n <= 0 || m <= 0 || d_v <= 0) return 0;
+    if (B <= 0 || H <= 0 || n <= 0 || m <= 0 || d_v <= 0 || n > kDecodeMaxRows) return 0;
     const int64_t bh = static_cast<int64_t>(B) * H;
     const int64_t cap = decode_split_cap(bh, m);
     if (cap == 1) return 0;
@@ -704,7 +703,7 @@ int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n
     if (B < 0 || H < 0 || n < 0 || m < 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_CACHE) return ATTN_ERR_INVALID_ARG;
     if (attn::mask_has_lengths(mask_kind) && key_lengths == nullptr) return ATTN_ERR_INVALID_ARG;
-    if (!head_dim_ok(d_k) || !head_dim_ok(d_v) || n > kDecodeMaxRows) return ATTN_ERR_UNSUPPORTED;
+    if (!head_dim_ok(d_k) || !head_dim_ok(d_v)) return ATTN_ERR_UNSUPPORTED;
     if (m > kMaxSeq) return ATTN_ERR_UNSUPPORTED;
     if (B == 0 || H == 0 || n == 0) return ATTN_OK;
     const int64_t bh = static_cast<int64_t>(B) * H;
@@ -722,11 +721,12 @@ int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n
     int rc0 = sm_count(&num_sms);
     if (rc0 != ATTN_OK) return rc0;
     const int64_t slots = static_cast<int64_t>(num_sms) * (d_k == 64 && d_v == 64 ? 2 : 1);
-    if (bh >= kDecodeTileWaves * slots && (slopes == nullptr || d_k == d_v)) {
-        // Enough (b, h) pairs to fill every SM several times over: the tensor-core
-        // forward kernel streams each pair's K and V once at the memory system's
-        // rate (its 128-row query tile is mostly padding, which the tensor cores
-        // absorb), and no chunk merge is needed.
+    if (n > kDecodeMaxRows || bh >= kDecodeTileWaves * slots) {
+        // More rows than the split kernel holds, or enough (b, h) pairs to fill
+        // every SM several times over: the tensor-core forward kernel streams each
+        // pair's K and V once at the memory system's rate (its 128-row query tile
+        // is mostly padding, which the tensor cores absorb), and no chunk merge is
+        // needed.
         uint32_t* status = nullptr;
         int rc = status_word(&status);
         if (rc != ATTN_OK) return rc;

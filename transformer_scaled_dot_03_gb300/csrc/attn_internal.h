@@ -113,8 +113,8 @@ cudaError_t launch_bwd_d64(int mask, const BwdMaps& maps, const BwdParams& p, cu
 cudaError_t launch_bwd_d128(int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 // Backward for d_k != d_v (64 and 128 either way round).
 cudaError_t launch_bwd_dmix(int d_k, int d_v, int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
-// Backward with the linear distance bias (p.slopes), d_k = d_v = d in {64, 128}.
-cudaError_t launch_bwd_alibi(int d, int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
+// Backward with the linear distance bias (p.slopes), d_k, d_v in {64, 128}.
+cudaError_t launch_bwd_alibi(int d_k, int d_v, int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 
 // Few-row forward (attn_kernel_decode.cuh): one CTA per (b, h, key chunk).
 struct DecodeParams {
@@ -168,8 +168,8 @@ cudaError_t launch_fwd_d128(int mask, int variant, const TensorMaps& maps, const
 // d_k != d_v (64 and 128 either way round), persistent kernel only.
 cudaError_t launch_fwd_dmix(int d_k, int d_v, int mask, const TensorMaps& maps, const FwdParams& p,
                             int num_sms, cudaStream_t stream);
-// Forward with the linear distance bias (p.slopes), d_k = d_v = d in {64, 128}.
-cudaError_t launch_fwd_alibi(int d, int mask, const TensorMaps& maps, const FwdParams& p, int num_sms,
+// Forward with the linear distance bias (p.slopes), d_k, d_v in {64, 128}.
+cudaError_t launch_fwd_alibi(int d_k, int d_v, int mask, const TensorMaps& maps, const FwdParams& p, int num_sms,
                              cudaStream_t stream);
 
 }  // namespace attn
