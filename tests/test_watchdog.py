@@ -46,3 +46,30 @@ def test_forced_timeout_reports_and_recovers(mask, d):
     Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale)
     assert np.abs(O.float().cpu().numpy() - Or).max() <= 1e-2
     assert np.abs(L.cpu().numpy() - Lr).max() <= 1e-3
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_forced_timeout_in_the_backward(d):
+    """The same for the backward kernels (the persistent pipelined one at d = 64, the
+    generic one at d = 128): the forced wait gives up, the status reports it, and a
+    normal backward afterwards matches the oracle."""
+    x = inputs.make_inputs(2, 2, 260, 260, d, d, "causal", seed=5100 + d)
+    dO = inputs.make_grad_output(2, 2, 260, d, seed=5101 + d)
+    Q, K, V, g = x.Q.cuda(), x.K.cuda(), x.V.cuda(), dO.cuda()
+    O, L = attn.attn_fwd(Q, K, V, x.mask, None, x.scale)
+    assert attn.device_status() == (attn.ATTN_OK, 0)
+    attn.set_watchdog(0, 1)
+    try:
+        attn.attn_bwd(Q, K, V, O, L, g, x.mask, None, x.scale)
+        rc, detail = attn.device_status()
+    finally:
+        attn.set_watchdog(0, 0)
+    assert rc == attn.ATTN_ERR_TIMEOUT
+    assert detail & FORCED_BIT
+    dQ, dK, dV = attn.attn_bwd(Q, K, V, O, L, g, x.mask, None, x.scale)
+    assert attn.device_status() == (attn.ATTN_OK, 0)
+    rq, rk, rv = oracle.attn_bwd(x.Q, x.K, x.V, dO, x.mask, None, x.scale)
+    for G, R in ((dQ, rq), (dK, rk), (dV, rv)):
+        G = G.float().cpu().numpy()
+        assert np.all(np.isfinite(G))
+        assert np.abs(G - R).max() <= 0.05 * max(1.0, np.abs(R).max())
