@@ -125,7 +125,7 @@ def attn_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, mask: str = "non
              want_lse: bool = True, stream=None):
     """Attention forward on the GPU. Q [B,H,n,d_k], K [B,H,m,d_k], V [B,H,m,d_v] bf16
     CUDA tensors (contiguous); ``key_lengths`` int32 CUDA [B] for the key-padding masks
-    ("key_padding", "causal_key_padding"). Returns (O [B,H,n,d_v] bf16, LSE [B,H,n] fp32
+    ("key_padding", "causal_key_padding", "causal_cache"). Returns (O [B,H,n,d_v] bf16, LSE [B,H,n] fp32
     or None). Asynchronous on ``stream`` (default: PyTorch's current stream)."""
     if mask not in MASK_CODES:
         raise ValueError(f"unknown mask {mask!r}")
