@@ -75,7 +75,36 @@ def pin_bias_and_linearity(plant=0):
         np.testing.assert_allclose(s[t], 2.0 * p1[t] - 3.0 * p2[t], atol=1e-11)
 
 
-PINS = [pin_loops, pin_round_trip, pin_bias_and_linearity]
+def pin_multihead_attention(plant=0):
+    """The whole multi-head self-attention of "第2章：完整的 Transformer 架构" §7.5
+    (nn.MultiheadAttention): the oracle's QKV projection and head split, attention and
+    head merge with W_O against torch's fp64 nn.MultiheadAttention with the same
+    weights (in_proj_weight is the stacked W_Q, W_K, W_V), with no mask, the causal
+    mask (attn_mask, True = masked) and key padding (key_padding_mask)."""
+    B, n, E, H = 2, 7, 12, 3
+    X = rnd((B, n, E), 20)
+    mha = torch.nn.MultiheadAttention(E, H, bias=True, batch_first=True, dtype=torch.float64)
+    with torch.no_grad():
+        for prm, seed in ((mha.in_proj_weight, 21), (mha.in_proj_bias, 22), (mha.out_proj.weight, 23),
+                          (mha.out_proj.bias, 24)):
+            prm.copy_(torch.from_numpy(rnd(tuple(prm.shape), seed)))
+    Xt = torch.from_numpy(X)
+    lens = [7, 4]
+    cases = {
+        "none": dict(),
+        "causal": dict(attn_mask=torch.ones(n, n, dtype=torch.bool).triu(1)),
+        "key_padding": dict(key_padding_mask=torch.arange(n)[None, :] >= torch.tensor(lens)[:, None]),
+    }
+    for mask, kw in cases.items():
+        with torch.no_grad():
+            ref, _ = mha(Xt, Xt, Xt, need_weights=False, **kw)
+        Q, K, V = oracle.proj_heads(X, mha.in_proj_weight.detach(), mha.in_proj_bias.detach(), H, 3, plant=plant)
+        O, _ = oracle.attn_fwd(Q, K, V, mask, key_lengths=lens if mask == "key_padding" else None)
+        Y = oracle.merge_proj(O, mha.out_proj.weight.detach(), mha.out_proj.bias.detach(), plant=plant)
+        np.testing.assert_allclose(Y, ref.numpy(), atol=1e-12, err_msg=mask)
+
+
+PINS = [pin_loops, pin_round_trip, pin_bias_and_linearity, pin_multihead_attention]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
