@@ -142,6 +142,15 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def quantile(xs, q):
+    """Linear-interpolation quantile of an ascending list."""
+    if len(xs) == 1:
+        return xs[0]
+    t = q * (len(xs) - 1)
+    i = min(int(t), len(xs) - 2)
+    return xs[i] + (xs[i + 1] - xs[i]) * (t - i)
+
+
 def reduce_over_ranks(ms, e2e_ms, world):
     """Slowest rank's device and end-to-end step times (replicas run independently;
     this host-side max is the only cross-rank operation)."""
@@ -312,16 +321,24 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter()
+        # an event between replays gives the spread of the step time over replays
+        ev_mid = [torch.cuda.Event(enable_timing=True) for _ in range(reps - 1)]
         with torch.cuda.stream(stream):
             ev0.record(stream)
-            for _ in range(reps):
+            for r in range(reps):
                 graph.replay()
+                if r < reps - 1:
+                    ev_mid[r].record(stream)
             ev1.record(stream)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall
         if world > 1:
             dist.barrier()
     dev_ms = ev0.elapsed_time(ev1)
+    bounds = [ev0] + ev_mid + [ev1]
+    per_step = sorted(bounds[r].elapsed_time(bounds[r + 1]) / G for r in range(reps))
+    spread = {"median": round(statistics.median(per_step), 6), "p10": round(quantile(per_step, 0.1), 6),
+              "p90": round(quantile(per_step, 0.9), 6), "over": f"{reps} graph replays of {G} steps"}
     rc, detail = attn.device_status(stream)
     if rc != attn.ATTN_OK:
         raise RuntimeError(f"device status {rc} ({detail}) after the timed region")
@@ -432,6 +449,7 @@ def run_ours(args):
             "metric": METRIC_BWD if bwd else (METRIC_PROJ[args.pass_] if proj else METRIC),
             "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": K_steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+            "ms_per_step_spread": spread,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded; bias-free Xavier projections of X~N(0,1))",
             "config": {"workload": w.name, "pass": args.pass_ if (bwd or proj) else ("decode" if decode else "fwd"),

@@ -47,3 +47,11 @@ def test_two_rank_timing_takes_the_slowest_rank():
 def test_single_rank_is_unchanged():
     assert bench.reduce_over_ranks(3.0, 4.0, 1) == (3.0, 4.0)
     assert bench.job_value(2e12, 1, 1.0) == pytest.approx(2000.0)   # 2 TFLOP in 1 ms
+
+
+def test_step_time_quantiles():
+    """The spread reported beside the step time: linear-interpolation quantiles."""
+    xs = [1.0, 2.0, 3.0, 4.0, 5.0]
+    assert bench.quantile(xs, 0.0) == 1.0 and bench.quantile(xs, 1.0) == 5.0
+    assert abs(bench.quantile(xs, 0.1) - 1.4) < 1e-12 and abs(bench.quantile(xs, 0.9) - 4.6) < 1e-12
+    assert bench.quantile([7.0], 0.9) == 7.0
