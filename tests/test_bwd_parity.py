@@ -53,14 +53,14 @@ def bounds(x: inputs.Inputs, dO: torch.Tensor, refs):
     Qd, Kd, Vd, g = (t.double().numpy() for t in (x.Q, x.K, x.V, dO))
     Or, _, W = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale, weights=True)
     A, _ = oracle.attn_fwd(x.Q, x.K, x.V.abs(), x.mask, x.key_lengths, x.scale)
-    dP = np.einsum("bhic,bhjc->bhij", g, Vd)
+    dP = np.einsum("bhic,bhjc->bhij", g, Vd, optimize=True)
     D = np.sum(g * Or, axis=-1)
     E = U * np.sum(np.abs(g) * (np.abs(Or) + A), axis=-1)
     T = W * (U * np.abs(dP - D[..., None]) + E[..., None])
     dQr, dKr, dVr = refs
-    bq = U * np.abs(dQr) + x.scale * np.einsum("bhij,bhjc->bhic", T, np.abs(Kd))
-    bk = U * np.abs(dKr) + x.scale * np.einsum("bhij,bhic->bhjc", T, np.abs(Qd))
-    bv = U * np.abs(dVr) + U * np.einsum("bhij,bhic->bhjc", W, np.abs(g))
+    bq = U * np.abs(dQr) + x.scale * np.einsum("bhij,bhjc->bhic", T, np.abs(Kd), optimize=True)
+    bk = U * np.abs(dKr) + x.scale * np.einsum("bhij,bhic->bhjc", T, np.abs(Qd), optimize=True)
+    bv = U * np.abs(dVr) + U * np.einsum("bhij,bhic->bhjc", W, np.abs(g), optimize=True)
     return bq, bk, bv
 
 
