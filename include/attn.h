@@ -140,9 +140,11 @@ int attn_get_device_status(void* stream, uint32_t* detail);
 /*
  * Watchdog settings for subsequent calls from any thread: `limit_ns` is the
  * wall-clock limit of one device-side wait (0 restores the default, 2 s).
- * `debug_flags` bit 0 makes every softmax warp wait on a barrier that nothing
- * completes, with a 20 ms limit, so that tests can exercise the timeout path
- * without a fault. Not meant to be changed while other threads launch.
+ * `debug_flags` bit 0 makes the warps that consume each kernel's results (the
+ * softmax warps of the forward, the compute warps of the backward, the consumer
+ * warps of the few-row decode kernel, the epilogue warps of the projections) wait
+ * on a barrier that nothing completes, with a 20 ms limit, so that tests can
+ * exercise the timeout path without a fault. Not meant to be changed while other threads launch.
  */
 void attn_set_watchdog(uint64_t limit_ns, uint32_t debug_flags);
 

@@ -73,3 +73,48 @@ def test_forced_timeout_in_the_backward(d):
         G = G.float().cpu().numpy()
         assert np.all(np.isfinite(G))
         assert np.abs(G - R).max() <= 0.05 * max(1.0, np.abs(R).max())
+
+
+def test_forced_timeout_in_the_decode_path():
+    """The few-row kernel split over key chunks (and the chunk merge after it): the
+    forced wait in its consumer warps gives up, the status reports it, and a normal
+    call afterwards matches the oracle."""
+    x = inputs.make_inputs(1, 2, 1, 4096, 128, 128, "none", seed=5200)
+    Q, K, V = x.Q.cuda(), x.K.cuda(), x.V.cuda()
+    assert attn.device_status() == (attn.ATTN_OK, 0)
+    attn.set_watchdog(0, 1)
+    try:
+        attn.attn_decode(Q, K, V, "none", None, x.scale)
+        rc, detail = attn.device_status()
+    finally:
+        attn.set_watchdog(0, 0)
+    assert rc == attn.ATTN_ERR_TIMEOUT
+    assert detail & FORCED_BIT
+    O, L = attn.attn_decode(Q, K, V, "none", None, x.scale)
+    assert attn.device_status() == (attn.ATTN_OK, 0)
+    Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, "none", None, x.scale)
+    assert np.abs(O.float().cpu().numpy() - Or).max() <= 1e-2
+    assert np.abs(L.cpu().numpy() - Lr).max() <= 1e-3
+
+
+def test_forced_timeout_in_the_projections():
+    """The projection kernel: the forced wait in its epilogue warps gives up, the MMA
+    warp drains what it issued before the tensor memory is released, the status
+    reports it, and a normal call afterwards matches the oracle."""
+    X = inputs.make_inputs(2, 1, 160, 1, 512, 512, seed=5300).Q[:, 0].contiguous()
+    W, bias = inputs.make_linear(3 * 512, 512, seed=5301, bias=True)
+    Xd, Wd, bd = X.cuda(), W.cuda(), bias.cuda()
+    assert attn.device_status() == (attn.ATTN_OK, 0)
+    attn.set_watchdog(0, 1)
+    try:
+        attn.proj_heads(Xd, Wd, 8, bd, 3)
+        rc, detail = attn.device_status()
+    finally:
+        attn.set_watchdog(0, 0)
+    assert rc == attn.ATTN_ERR_TIMEOUT
+    assert detail & FORCED_BIT
+    outs = attn.proj_heads(Xd, Wd, 8, bd, 3)
+    assert attn.device_status() == (attn.ATTN_OK, 0)
+    refs = oracle.proj_heads(X, W, bias, 8, 3)
+    for got, ref in zip(outs, refs):
+        assert np.abs(got.float().cpu().numpy() - ref).max() <= 2e-2 * max(1.0, np.abs(ref).max())

@@ -769,6 +769,7 @@ int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n
     p.slopes = slopes;
     p.status = status;
     p.watchdog_ns = g_watchdog_ns;
+    p.debug_flags = g_debug_flags;
     cudaError_t e = attn::launch_decode(d_k, d_v, decode_rows(n), tmK, tmV, p, st);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("decode kernel launch", e);
 }
@@ -847,6 +848,7 @@ int run_proj(bool heads_in, bool heads_out, attn::ProjMaps& maps, attn::ProjPara
     p.tiles_n = (p.N + 255) / 256;
     p.status = status;
     p.watchdog_ns = g_watchdog_ns;
+    p.debug_flags = g_debug_flags;
     cudaError_t e = attn::launch_proj(heads_in, heads_out, maps, p, num_sms, st);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("projection kernel launch", e);
 }

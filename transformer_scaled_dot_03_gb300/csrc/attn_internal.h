@@ -133,6 +133,7 @@ struct DecodeParams {
     const float* slopes;          // fp32 [H]: distance-bias slope per head, or null (no bias)
     uint32_t* status;
     uint64_t watchdog_ns;
+    uint32_t debug_flags;
 };
 
 // rows: the kernel variant handles n <= rows (1, 2, 4 or 8).
@@ -149,6 +150,7 @@ struct ProjParams {
     const uint16_t* bias;         // bf16 [N] or null
     uint32_t* status;
     uint64_t watchdog_ns;
+    uint32_t debug_flags;
 };
 
 struct ProjMaps {

@@ -64,7 +64,8 @@ struct Layout {
     static constexpr int BAR_OFF = RED_OFF + 4 * RED_WARP;
     static constexpr int B_FULL = 0;
     static constexpr int B_EMPTY = STAGES;
-    static constexpr int NBARS = 2 * STAGES;
+    static constexpr int B_NEVER = 2 * STAGES;               // debug: completed by nothing
+    static constexpr int NBARS = B_NEVER + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16 + 1024;
     static_assert(BYTES * CTAS_PER_SM <= 232448, "shared memory budget");
@@ -122,6 +123,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
             mbar_init(bar(L::B_FULL + s), 1);
             mbar_init(bar(L::B_EMPTY + s), 4);
         }
+        mbar_init(bar(L::B_NEVER), 1);
         *abort_word = 0u;
         fence_mbar_init();
     }
@@ -185,7 +187,11 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     const float sb = p.slopes != nullptr ? __ldg(p.slopes + bh % p.H) * LOG2E : 0.f;
     const int row = 32 * warp + lane;       // this lane's key row within a tile
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
+    if (p.debug_flags & DEBUG_FORCE_TIMEOUT) {
+        ok = mbar_wait(bar(L::B_NEVER), 0, abort_word, p.status, STATUS_FORCED, 20000000ull);
+        ok = __all_sync(0xffffffffu, ok);
+    }
+    for (int t = 0; ok && t < ntiles; ++t) {
         const int s = t % L::STAGES;
         ok = mbar_wait(bar(L::B_FULL + s), static_cast<uint32_t>(t / L::STAGES) & 1u, abort_word, p.status,
                        STATUS_SOFTMAX_WAIT, limit);

@@ -58,7 +58,9 @@ constexpr int B_FULL = 0;
 constexpr int B_EMPTY = STAGES;
 constexpr int B_ACC_FULL = 2 * STAGES;
 constexpr int B_ACC_EMPTY = B_ACC_FULL + 2;
-constexpr int NBARS = B_ACC_EMPTY + 2;
+constexpr int B_DRAIN = B_ACC_EMPTY + 2;        // every MMA issued is complete   (commit)
+constexpr int B_NEVER = B_DRAIN + 1;            // debug: completed by nothing
+constexpr int NBARS = B_NEVER + 1;
 constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
 constexpr int BYTES = MISC_OFF + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
@@ -91,6 +93,8 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
             mbar_init(bar(B_ACC_FULL + a), 1);
             mbar_init(bar(B_ACC_EMPTY + a), 128);
         }
+        mbar_init(bar(B_DRAIN), 1);
+        mbar_init(bar(B_NEVER), 1);
         *abort_word = 0u;
         fence_mbar_init();
     }
@@ -195,6 +199,12 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
             if (!ok) break;
             mma_commit_warp(bar(B_ACC_FULL + acc));
         }
+        // every MMA issued completes before the tensor memory is released (after an
+        // abort some may still be running)
+        mma_commit_warp(bar(B_DRAIN));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_test(bar(B_DRAIN), 0) && globaltimer_ns() - t0 < 100000000ull) {
+        }
         __syncwarp();
     } else {
         // ================================================== epilogue (warps 0-3, thread = row)
@@ -202,6 +212,10 @@ attn_proj_kernel(const __grid_constant__ ProjMaps maps, const ProjParams p)
         const uint32_t st0 = sbase + ST_OFF + static_cast<uint32_t>(warp) * 2 * ST_BYTES;
         int tl = 0, piece_count = 0;
         bool ok = true;
+        if (p.debug_flags & DEBUG_FORCE_TIMEOUT) {
+            ok = mbar_wait(bar(B_NEVER), 0, abort_word, p.status, STATUS_FORCED, 20000000ull);
+            ok = __all_sync(0xffffffffu, ok);
+        }
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tl) {
             const int acc = tl & 1;
             const int m0 = (tile / p.tiles_n) * BM;
