@@ -50,8 +50,12 @@
  *     runtime; a device-side watchdog expiry is reported by
  *     attn_get_device_status().
  *   - Memory: the library allocates one 4-byte device status word per device
- *     on the first call on that device and nothing else.
- *   - Thread safety: concurrent calls on distinct streams are safe.
+ *     on the first call on that device and nothing else. The exception is
+ *     attn_fwd_noalloc, which allocates nothing (its status word sits in a
+ *     fixed array inside the library; see its comment).
+ *   - Thread safety: concurrent calls on distinct streams are safe. The status
+ *     words are shared by every call on a device, so attn_get_device_status
+ *     reports a timeout of any call on the device, whichever stream it ran on.
  */
 #ifndef ATTN_SM103A_H
 #define ATTN_SM103A_H
@@ -130,12 +134,21 @@ int attn_fwd_alibi(const void* Q, const void* K, const void* V, int B, int H, in
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
- * word. Returns ATTN_ERR_TIMEOUT if any kernel since the last call gave up on a
- * bounded wait (its outputs are then undefined), ATTN_ERR_CUDA if the
- * synchronisation failed, else ATTN_OK. If `detail` is not NULL it receives the
- * raw status bits (which wait gave up).
+ * words: the one attn_fwd and the other entry points use, and the one inside
+ * the array of attn_fwd_noalloc. Returns ATTN_ERR_TIMEOUT if any kernel since
+ * the last call gave up on a bounded wait (its outputs are then undefined),
+ * ATTN_ERR_CUDA if the synchronisation or the read failed, else ATTN_OK. It
+ * allocates no device memory (a word that no call has created yet reads as
+ * zero). Kernels still running on other streams may set a bit after the read;
+ * synchronise them first for a complete report.
  */
-int attn_get_device_status(void* stream, uint32_t* detail);
+int attn_get_device_status(void* stream);
+
+/*
+ * The raw status bits (which kind of wait gave up) that the calling thread's
+ * last attn_get_device_status read; 0 if it reported ATTN_OK.
+ */
+uint32_t attn_last_status_detail(void);
 
 /*
  * Watchdog settings for subsequent calls from any thread: `limit_ns` is the
@@ -150,28 +163,30 @@ void attn_set_watchdog(uint64_t limit_ns, uint32_t debug_flags);
 
 /*
  * attn_fwd without device memory allocation. The pages have no counterpart to
- * this entry point; it exists for callers that may not call cudaMalloc, such
- * as code running while another component owns every device allocation (a
- * pooled or caching allocator, a fixed memory budget) or code that must not
- * add device allocations once it is running.
+ * this entry point. It is for callers that may not call cudaMalloc: code that
+ * runs while another component owns every device allocation (a pooled or
+ * caching allocator with a fixed budget), or code that must not add device
+ * allocations once it is running.
  *
- * Arguments, layouts, results and status codes are those of attn_fwd. The
- * difference is the kernel's scratch memory: attn_fwd allocates its 4-byte
- * device status word on first use, while this entry point takes its scratch
- * from a fixed 256-byte device array inside the library (every GPU that loads
- * the library keeps it until the process exits). One call needs 4 bytes of it
- * whatever the problem sizes; a need beyond the 256 bytes would be refused
- * with ATTN_ERR_UNSUPPORTED. No call allocates or frees device memory.
+ * Arguments, layouts, results and status codes are those of attn_fwd. The only
+ * difference is where the kernel's scratch memory lives. attn_fwd allocates
+ * its 4-byte device status word on its first call on a device; this entry
+ * point uses the first word of a fixed 256-byte device array inside the
+ * library instead (every GPU that loads the library holds the array until the
+ * process exits). One call needs those 4 bytes whatever the problem sizes, so
+ * no size is refused for want of scratch. No call allocates or frees device
+ * memory, and neither does attn_get_device_status.
  *
- *   - The first call on each device looks up the array's device address (a
- *     cudaGetSymbolAddress on that device); make that first call before any
+ *   - The first call on each device looks up the array's device address with
+ *     cudaGetSymbolAddress on that device. Make that first call before any
  *     stream capture on the device.
- *   - All calls share the array. Each call resets the status word to zero on
- *     `stream` before its kernel, so calls whose kernels overlap on the GPU
- *     (different streams, no ordering between them) race on it.
- *   - A device-side watchdog expiry is recorded in the shared array only; it
- *     is not reported by attn_get_device_status. Use attn_fwd when that report
- *     is needed.
+ *   - All calls share the array. The kernel only sets bits in the status word
+ *     and never reads it, so the word needs no reset between calls: it is zero
+ *     when the library loads, and attn_get_device_status reads and clears it
+ *     together with attn_fwd's word. Calls that overlap on the GPU (different
+ *     streams, no ordering between them) race on this word: a timeout in one
+ *     is reported for all of them, and a clear issued while one is running can
+ *     drop its bit.
  */
 int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int B, int H, int n, int m, int d_k,
                      int d_v, int mask_kind, const int32_t* key_lengths, float scale, void* O,

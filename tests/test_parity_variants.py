@@ -72,29 +72,17 @@ def test_variant_rescaling(mask, n, m):
     check_full(x, f"x8 {mask} n={n} m={m}", format_aware=True)
 
 
-def test_decoder_target_mask_full_size_sampled():
-    """Big-decoder sizes (B 16, H 16, n = m = 1024, d 64) under the decoder target mask
-    with key lengths drawn in [512, 1024]; the oracle computes a seeded sample of rows."""
-    B, H, n, d = 16, 16, 1024, 64
-    x = inputs.make_inputs(B, H, n, n, d, d, "causal_key_padding", seed=7200, len_lo=512, len_hi=n)
+@pytest.mark.parametrize("name", ["decoder_target_mask", "prefill_continuation", "wide_values"])
+def test_variant_workload_every_row(name):
+    """The variant workloads at full size: the decoder target mask at big-decoder sizes
+    (B 16, H 16, n = m = 1024, d 64, key lengths in [512, 1024]); 1024 new query rows
+    against 8192 keys at d 128 (causal, bottom-right); value heads of 128 against key
+    heads of 64. Every row against the oracle."""
+    w = inputs.WORKLOADS[name]
+    x = inputs.workload_inputs(w)
     O, L = run_gpu(x)
-    rows = inputs.sample_rows(B, H, n, 4000, seed=7201)
-    Or, Lr = oracle.attn_rows(x.Q, x.K, x.V, rows, x.mask, x.key_lengths, x.scale)
-    r = rows.numpy()
-    compare(O.reshape(-1, d)[r], L.reshape(-1)[r], Or, Lr, "decoder target mask")
-    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
-
-
-def test_prefill_continuation_sampled():
-    """512 new query rows against 8192 keys at d 128 (causal, bottom-right): every row
-    sees at least 7681 keys; sampled rows against the oracle."""
-    B, H, n, m, d = 2, 8, 512, 8192, 128
-    x = inputs.make_inputs(B, H, n, m, d, d, "causal", seed=7300, value_scale=0.5)
-    O, L = run_gpu(x)
-    rows = inputs.sample_rows(B, H, n, 1500, seed=7301)
-    Or, Lr = oracle.attn_rows(x.Q, x.K, x.V, rows, x.mask, None, x.scale)
-    r = rows.numpy()
-    compare(O.reshape(-1, d)[r], L.reshape(-1)[r], Or, Lr, "prefill continuation")
+    Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale, threads=oracle.default_threads())
+    compare(O, L, Or, Lr, name)
 
 
 def test_causal_suffix_on_gpu():

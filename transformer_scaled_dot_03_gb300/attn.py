@@ -32,8 +32,9 @@ MASK_CODES = {_inputs.MASK_NONE: 0, _inputs.MASK_CAUSAL: 1, _inputs.MASK_KEY_PAD
               _inputs.MASK_CAUSAL_KEY_PADDING: 3, _inputs.MASK_CAUSAL_CACHE: 4}
 
 # Every symbol include/attn.h declares.
-EXPORTS = ("attn_fwd", "attn_fwd_alibi", "attn_decode_alibi", "attn_bwd_alibi", "attn_get_device_status", "attn_set_watchdog", "attn_status_string",
-           "attn_last_error", "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
+EXPORTS = ("attn_fwd", "attn_fwd_alibi", "attn_decode_alibi", "attn_bwd_alibi", "attn_get_device_status",
+           "attn_last_status_detail", "attn_set_watchdog", "attn_status_string", "attn_last_error",
+           "attn_fwd_noalloc", "attn_bwd", "attn_bwd_workspace_size", "attn_decode",
            "attn_decode_workspace_size", "attn_proj_heads", "attn_merge_proj")
 
 _lock = threading.Lock()
@@ -61,8 +62,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_fwd.restype = i32
         lib.attn_fwd_alibi.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, f32, vp, vp, vp]
         lib.attn_fwd_alibi.restype = i32
-        lib.attn_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        lib.attn_get_device_status.argtypes = [vp]
         lib.attn_get_device_status.restype = i32
+        lib.attn_last_status_detail.argtypes = []
+        lib.attn_last_status_detail.restype = ctypes.c_uint32
+        lib.attn_fwd_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp, vp]
+        lib.attn_fwd_noalloc.restype = i32
         lib.attn_set_watchdog.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
         lib.attn_set_watchdog.restype = None
         lib.attn_status_string.argtypes = [i32]
@@ -377,10 +382,11 @@ def merge_proj(O: torch.Tensor, W_o: torch.Tensor, bias: torch.Tensor | None = N
 
 
 def device_status(stream=None) -> tuple[int, int]:
-    """Synchronise the stream; return (status, detail bits) of the device status word."""
-    detail = ctypes.c_uint32(0)
-    rc = load().attn_get_device_status(ctypes.c_void_p(_stream_handle(stream)), ctypes.byref(detail))
-    return rc, int(detail.value)
+    """Synchronise the stream, read and clear the device's status words; return
+    (status, detail bits)."""
+    lib = load()
+    rc = lib.attn_get_device_status(ctypes.c_void_p(_stream_handle(stream)))
+    return rc, int(lib.attn_last_status_detail())
 
 
 def set_watchdog(limit_ns: int = 0, debug_flags: int = 0) -> None:

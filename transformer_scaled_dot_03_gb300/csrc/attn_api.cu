@@ -30,6 +30,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 uint64_t g_watchdog_ns = kDefaultWatchdogNs;
 uint32_t g_debug_flags = 0;
 thread_local char g_last_error[256] = "";
+thread_local uint32_t g_last_detail = 0;   // bits read by this thread's last attn_get_device_status
 
 int fail_cuda(const char* what, cudaError_t e)
 {
@@ -61,6 +62,18 @@ int status_word(uint32_t** out)
         if (e != cudaSuccess) return fail_cuda("cudaDeviceSynchronize", e);
         g_status[dev] = p;
     }
+    *out = g_status[dev];
+    return ATTN_OK;
+}
+
+// The current device's status word if it exists (no allocation); null otherwise.
+int existing_status_word(uint32_t** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return fail_msg("device index out of range");
+    std::lock_guard<std::mutex> lk(g_mu);
     *out = g_status[dev];
     return ATTN_OK;
 }
@@ -153,25 +166,6 @@ int sm_count(int* out)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Kernel variant. Default: the persistent kernel with P apart from S
-// (KERNEL_DP). ATTN_KERNEL=dp|nt1|nt2 overrides it (a tuning knob for
-// measurements, read once); the NT variants only take d_k = d_v and the masks
-// none, causal with n = m, and key padding, so other calls keep KERNEL_DP.
-int kernel_variant(int d_k, int d_v, int mask_kind, int n, int m)
-{
-    static int env = [] {
-        const char* v = std::getenv("ATTN_KERNEL");
-        if (v == nullptr) return -1;
-        if (std::strcmp(v, "dp") == 0) return static_cast<int>(attn::KERNEL_DP);
-        if (std::strcmp(v, "nt1") == 0) return static_cast<int>(attn::KERNEL_NT1);
-        if (std::strcmp(v, "nt2") == 0) return static_cast<int>(attn::KERNEL_NT2);
-        return -1;
-    }();
-    const bool nt_ok = d_k == d_v && mask_kind != ATTN_MASK_CAUSAL_KEY_PADDING && mask_kind != ATTN_MASK_CAUSAL_CACHE &&
-                       !(mask_kind == ATTN_MASK_CAUSAL && n != m);
-    return (env >= 0 && nt_ok) ? env : static_cast<int>(attn::KERNEL_DP);
-}
-
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
 
 // Host-side checks shared by both entry points.
@@ -191,7 +185,7 @@ int validate(const void* Q, const void* K, const void* V, int B, int H, int n, i
     if ((LSE != nullptr && !aligned(LSE, 4)) || (key_lengths != nullptr && !aligned(key_lengths, 4)))
         return ATTN_ERR_MISALIGNED;
     const int64_t bh = static_cast<int64_t>(B) * H;
-    const int64_t num_qblocks = (static_cast<int64_t>(n) + 255) / 128;   // worst case over the variants
+    const int64_t num_qblocks = (static_cast<int64_t>(n) + 127) / 128;
     if (bh > INT32_MAX || bh * num_qblocks > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
@@ -215,9 +209,7 @@ int launch_attention(const void* Q, const void* K, const void* V, int B, int H, 
                      uint32_t* status, cudaStream_t st, const float* slopes = nullptr)
 {
     const int64_t bh = static_cast<int64_t>(B) * H;
-    const int variant = slopes != nullptr ? static_cast<int>(attn::KERNEL_DP) : kernel_variant(d_k, d_v, mask_kind, n, m);
-    const int64_t rows_per_cta = attn::kernel_rows_per_cta(variant);
-    const int64_t num_qblocks = (static_cast<int64_t>(n) + rows_per_cta - 1) / rows_per_cta;
+    const int64_t num_qblocks = (static_cast<int64_t>(n) + 127) / 128;
 
     PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
     int rc = encoder(&enc);
@@ -230,7 +222,7 @@ int launch_attention(const void* Q, const void* K, const void* V, int B, int H, 
 
     const double sc = (scale > 0.f && std::isfinite(scale)) ? static_cast<double>(scale)
                                                              : 1.0 / std::sqrt(static_cast<double>(d_k));
-    const bool paired = variant == attn::KERNEL_DP && attn::mask_is_causal(mask_kind);
+    const bool paired = attn::mask_is_causal(mask_kind);   // causal units pair two query tiles
     attn::FwdParams p;
     p.B = B;
     p.H = H;
@@ -250,17 +242,86 @@ int launch_attention(const void* Q, const void* K, const void* V, int B, int H, 
 
     int num_sms = 0;
     if ((rc = sm_count(&num_sms)) != ATTN_OK) return rc;
-    const int64_t ctas = bh * num_qblocks;
     cudaError_t e;
     if (slopes != nullptr)
         e = attn::launch_fwd_alibi(d_k, d_v, mask_kind, maps, p, num_sms, st);
     else if (d_k != d_v)
         e = attn::launch_fwd_dmix(d_k, d_v, mask_kind, maps, p, num_sms, st);
     else if (d_k == 64)
-        e = attn::launch_fwd_d64(mask_kind, variant, maps, p, ctas, num_sms, st);
+        e = attn::launch_fwd_d64(mask_kind, maps, p, num_sms, st);
     else
-        e = attn::launch_fwd_d128(mask_kind, variant, maps, p, ctas, num_sms, st);
+        e = attn::launch_fwd_d128(mask_kind, maps, p, num_sms, st);
     return e == cudaSuccess ? ATTN_OK : fail_cuda("attention kernel launch", e);
+}
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that may not allocate device memory.
+//
+// attn_fwd keeps its device status word (the kernel's only scratch memory) in
+// a 4-byte cudaMalloc made on the first call on each device. Some callers
+// cannot allow that: code that runs while another component owns every
+// allocation (a caching or pooled allocator, a fixed memory budget), or code
+// that must not add device allocations after start-up. attn_fwd_noalloc runs
+// the same kernel with its scratch taken from this file-scope device array.
+
+// The array's stated size. One call uses its first word as the kernel's status
+// word, whatever the problem sizes (the forward kernel needs no other scratch).
+constexpr size_t kNoAllocScratchBytes = 256;
+constexpr size_t kNoAllocStatusBytes = sizeof(uint32_t);
+static_assert(kNoAllocStatusBytes <= kNoAllocScratchBytes, "scratch layout");
+
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint32_t)];
+
+std::mutex g_noalloc_mu;
+uint32_t* g_noalloc_addr[kMaxDevices] = {};   // device address of the array, per device
+
+// Device address of the scratch array on the current device, looked up once
+// per device. In host code the array's name is only a host-side stand-in.
+int noalloc_scratch(uint32_t** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return fail_msg("device index out of range");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return fail_cuda("cudaGetSymbolAddress(no-allocation scratch)", e);
+        if (ptr == nullptr) return fail_msg("no-allocation scratch has no device address");
+        g_noalloc_addr[dev] = static_cast<uint32_t*>(ptr);
+    }
+    *out = g_noalloc_addr[dev];
+    return ATTN_OK;
+}
+
+// The array's device address on the current device if a call has looked it up
+// there already; null otherwise.
+int existing_noalloc_scratch(uint32_t** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
+    if (dev < 0 || dev >= kMaxDevices) return fail_msg("device index out of range");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    *out = g_noalloc_addr[dev];
+    return ATTN_OK;
+}
+
+// Reads a device status word and, if it is non-zero, clears it on `st`.
+int read_and_clear(uint32_t* word, cudaStream_t st, uint32_t* value)
+{
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpy(&v, word, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda("cudaMemcpy(status word)", e);
+    if (v != 0) {
+        e = cudaMemsetAsync(word, 0, sizeof(uint32_t), st);
+        if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(status word)", e);
+        e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return fail_cuda("cudaStreamSynchronize", e);
+    }
+    *value = v;
+    return ATTN_OK;
 }
 
 }  // namespace
@@ -296,25 +357,30 @@ int attn_fwd_alibi(const void* Q, const void* K, const void* V, int B, int H, in
                             slopes);
 }
 
-int attn_get_device_status(void* stream, uint32_t* detail)
+int attn_get_device_status(void* stream)
 {
-    uint32_t* status = nullptr;
-    int rc = status_word(&status);
-    if (rc != ATTN_OK) return rc;
-    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    g_last_detail = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return fail_cuda("cudaStreamSynchronize", e);
-    uint32_t v = 0;
-    e = cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return fail_cuda("cudaMemcpy(status word)", e);
-    if (v != 0) {
-        e = cudaMemsetAsync(status, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(status word)", e);
-        e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return fail_cuda("cudaStreamSynchronize", e);
+    // attn_fwd's word (absent until a call created it) and the word in the
+    // no-allocation entry point's array (known once a call looked it up)
+    uint32_t* words[2] = {nullptr, nullptr};
+    int rc = existing_status_word(&words[0]);
+    if (rc == ATTN_OK) rc = existing_noalloc_scratch(&words[1]);
+    if (rc != ATTN_OK) return rc;
+    uint32_t bits = 0;
+    for (uint32_t* w : words) {
+        if (w == nullptr) continue;
+        uint32_t v = 0;
+        if ((rc = read_and_clear(w, st, &v)) != ATTN_OK) return rc;
+        bits |= v;
     }
-    if (detail != nullptr) *detail = v;
-    return v != 0 ? ATTN_ERR_TIMEOUT : ATTN_OK;
+    g_last_detail = bits;
+    return bits != 0 ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
+
+uint32_t attn_last_status_detail(void) { return g_last_detail; }
 
 void attn_set_watchdog(uint64_t limit_ns, uint32_t debug_flags)
 {
@@ -339,69 +405,19 @@ const char* attn_last_error(void) { return g_last_error; }
 
 }  // extern "C"
 
-// ---------------------------------------------------------------------------
-// Entry point for callers that may not allocate device memory.
-//
-// attn_fwd keeps its device status word (the kernel's only scratch memory) in
-// a 4-byte cudaMalloc made on the first call on each device. Some callers
-// cannot allow that: code that runs while another component owns every
-// allocation (a caching or pooled allocator, a fixed memory budget), or code
-// that must not add device allocations after start-up. attn_fwd_noalloc runs
-// the same kernel with its scratch taken from this file-scope device array.
-namespace {
-
-constexpr size_t kNoAllocScratchBytes = 256;                  // stated maximum
-constexpr size_t kNoAllocStatusBytes = sizeof(uint32_t);      // scratch one call needs
-static_assert(kNoAllocStatusBytes <= kNoAllocScratchBytes, "scratch layout");
-
-static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocScratchBytes / sizeof(uint32_t)];
-
-std::mutex g_noalloc_mu;
-uint32_t* g_noalloc_addr[kMaxDevices] = {};   // device address of the array, per device
-
-// Device address of the scratch array on the current device, looked up once
-// per device. In host code the array's name is only a host-side stand-in.
-int noalloc_scratch(uint32_t** out)
-{
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail_cuda("cudaGetDevice", e);
-    if (dev < 0 || dev >= kMaxDevices) return fail_msg("device index out of range");
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
-        void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess) return fail_cuda("cudaGetSymbolAddress(no-allocation scratch)", e);
-        if (ptr == nullptr) return fail_msg("no-allocation scratch has no device address");
-        g_noalloc_addr[dev] = static_cast<uint32_t*>(ptr);
-    }
-    *out = g_noalloc_addr[dev];
-    return ATTN_OK;
-}
-
-}  // namespace
-
 extern "C" int attn_fwd_noalloc(const void* Q, const void* K, const void* V, int B, int H, int n, int m,
                                 int d_k, int d_v, int mask_kind, const int32_t* key_lengths, float scale,
                                 void* O, float* LSE, void* stream)
 {
     int rc = validate(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, O, LSE);
     if (rc != ATTN_OK || B == 0 || H == 0 || n == 0) return rc;
-    // The kernel's scratch for one call is the status word, whatever the sizes;
-    // anything larger than the array would be refused here.
-    if (kNoAllocStatusBytes > kNoAllocScratchBytes) {
-        snprintf(g_last_error, sizeof(g_last_error), "attn_fwd_noalloc: scratch need %zu B exceeds %zu B",
-                 kNoAllocStatusBytes, kNoAllocScratchBytes);
-        return ATTN_ERR_UNSUPPORTED;
-    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (m == 0) return fill_no_keys(static_cast<int64_t>(B) * H, n, d_v, O, LSE, st);
-
     uint32_t* scratch = nullptr;
     if ((rc = noalloc_scratch(&scratch)) != ATTN_OK) return rc;
-    // the status word must start at zero; it keeps the previous call's value otherwise
-    cudaError_t e = cudaMemsetAsync(scratch, 0, kNoAllocStatusBytes, st);
-    if (e != cudaSuccess) return fail_cuda("cudaMemsetAsync(no-allocation scratch)", e);
+    // The kernel only ORs bits into its status word and never reads it back, so the
+    // word needs no reset before a call: it starts at zero when the module loads and
+    // attn_get_device_status clears it once it has read it (like attn_fwd's word).
     return launch_attention(Q, K, V, B, H, n, m, d_k, d_v, mask_kind, key_lengths, scale, O, LSE, scratch, st);
 }
 

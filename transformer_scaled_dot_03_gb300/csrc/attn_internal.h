@@ -40,7 +40,7 @@ struct FwdParams {
     int B, H, n, m;
     int causal_off;               // m - n: query row i sees keys j <= i + causal_off (causal masks)
     int num_qblocks;              // ceil(n / rows per work unit)
-    int num_units;                // B * H * num_qblocks (persistent kernel)
+    int num_units;                // work units (query tiles, paired under the causal masks)
     void* O;                      // bf16 [B,H,n,d_v] (persistent kernel stores rows directly)
     const int32_t* key_lengths;   // device int32 [B] (key-padding masks only)
     float scale_log2;             // scale * log2(e)
@@ -76,14 +76,6 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
-
-// Kernel variants (see the kernel headers):
-//   KERNEL_DP   one query tile per CTA, P apart from S in tensor memory
-//   KERNEL_NT1  one query tile per CTA, P over S
-//   KERNEL_NT2  two query tiles per CTA, P over S
-enum { KERNEL_DP = 0, KERNEL_NT1 = 1, KERNEL_NT2 = 2 };
-
-inline int kernel_rows_per_cta(int variant) { return variant == KERNEL_NT2 ? 256 : 128; }
 
 // Backward (attn_kernel_bwd.cuh): one CTA per (b, h, 128-key tile).
 struct BwdParams {
@@ -161,13 +153,10 @@ struct ProjMaps {
 cudaError_t launch_proj(bool heads_in, bool heads_out, const ProjMaps& maps, const ProjParams& p, int num_sms,
                         cudaStream_t stream);
 
-// num_ctas: grid of the one-unit-per-CTA variants; num_sms sizes the persistent grid.
-// The NT variants take d_k = d_v, masks none / causal (n = m) / key padding.
-cudaError_t launch_fwd_d64(int mask, int variant, const TensorMaps& maps, const FwdParams& p,
-                           int64_t num_ctas, int num_sms, cudaStream_t stream);
-cudaError_t launch_fwd_d128(int mask, int variant, const TensorMaps& maps, const FwdParams& p,
-                            int64_t num_ctas, int num_sms, cudaStream_t stream);
-// d_k != d_v (64 and 128 either way round), persistent kernel only.
+// The persistent forward kernel; num_sms sizes its grid.
+cudaError_t launch_fwd_d64(int mask, const TensorMaps& maps, const FwdParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_fwd_d128(int mask, const TensorMaps& maps, const FwdParams& p, int num_sms, cudaStream_t stream);
+// d_k != d_v (64 and 128 either way round).
 cudaError_t launch_fwd_dmix(int d_k, int d_v, int mask, const TensorMaps& maps, const FwdParams& p,
                             int num_sms, cudaStream_t stream);
 // Forward with the linear distance bias (p.slopes), d_k, d_v in {64, 128}.
