@@ -44,7 +44,7 @@ def run_decode(x: inputs.Inputs):
 def check(x, label):
     O, L = run_decode(x)
     Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale)
-    return compare(O, L, Or, Lr, label)
+    return compare(O, L, Or, Lr, label, x=x)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -120,7 +120,7 @@ def test_decode_workloads_every_row(name):
     x = inputs.workload_inputs(w)
     O, L = run_decode(x)
     Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale, threads=oracle.default_threads())
-    compare(O, L, Or, Lr, name)
+    compare(O, L, Or, Lr, name, x=x)
 
 
 def test_decode_m_zero():

@@ -82,7 +82,7 @@ def test_variant_workload_every_row(name):
     x = inputs.workload_inputs(w)
     O, L = run_gpu(x)
     Or, Lr = oracle.attn_fwd(x.Q, x.K, x.V, x.mask, x.key_lengths, x.scale, threads=oracle.default_threads())
-    compare(O, L, Or, Lr, name)
+    compare(O, L, Or, Lr, name, x=x)
 
 
 def test_causal_suffix_on_gpu():
