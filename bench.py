@@ -67,6 +67,7 @@ def peaks():
 
 
 KERNEL_SOURCES = ["transformer_scaled_dot_03_gb300/csrc/attn_kernel_dp.cuh",
+                  "transformer_scaled_dot_03_gb300/csrc/attn_softmax.cuh",
                   "transformer_scaled_dot_03_gb300/csrc/sm103a.cuh",
                   "transformer_scaled_dot_03_gb300/csrc/attn_internal.h"]
 
@@ -630,6 +631,30 @@ def run_reference(args):
             "wall_s": round(sum(secs), 2)}
 
 
+def run_launches(args):
+    """Untimed launches of the pass on the workload's inputs, for a profiler to
+    capture (no timing, no JSON line)."""
+    from transformer_scaled_dot_03_gb300 import attn, build
+    build.build()
+    attn.load()
+    w, x = make_workload(args.workload)
+    dev = torch.device("cuda", 0)
+    Q, K, V = x.Q.to(dev), x.K.to(dev), x.V.to(dev)
+    lens = x.key_lengths.to(dev) if x.key_lengths is not None else None
+    slopes = workload_slopes(w).to(dev) if w.alibi else None
+    for _ in range(args.launches):
+        if w.path == "decode":
+            attn.attn_decode(Q, K, V, w.mask, lens, x.scale)
+        elif slopes is not None:
+            attn.attn_fwd_alibi(Q, K, V, slopes, w.mask, lens, x.scale)
+        else:
+            attn.attn_fwd(Q, K, V, w.mask, lens, x.scale)
+    rc, detail = attn.device_status()
+    if rc != attn.ATTN_OK:
+        raise RuntimeError(f"device status {rc} ({detail})")
+    print(f"{args.launches} launches of {w.name}: ok", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -645,6 +670,8 @@ def main():
                          "proj / outproj: the projections around it (weights resident)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launches", type=int, default=0,
+                    help="only run this many untimed forward launches on the workload (for profilers)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
     args = ap.parse_args()
@@ -652,6 +679,9 @@ def main():
         ap.error("--warmup must be >= 3")
     if not 1 <= args.steps <= MAX_GRAPH_STEPS:
         ap.error(f"--steps must be in [1, {MAX_GRAPH_STEPS}]")
+    if args.launches > 0:
+        run_launches(args)
+        return
     res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
