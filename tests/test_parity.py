@@ -194,6 +194,20 @@ def test_key_padding_lengths(d, m, lens):
     check_full(x, f"key_padding m={m} lens={lens} d={d}")
 
 
+@pytest.mark.parametrize("d,ctas_per_sm", [(64, 2), (128, 1)])
+def test_empty_tiles_between_tiles_with_keys(d, ctas_per_sm):
+    """A CTA whose work units run (keys, no keys, keys): one 128-row tile per
+    sequence, G = SMs x CTAs per SM persistent CTAs taking units c, c + G, c + 2G,
+    and the sequences [G, 2G) of length 0. At d = 128 each tile's Q is copied into
+    tensor memory one tile ahead; the tile without keys must not copy its
+    successor's Q a second time."""
+    G = torch.cuda.get_device_properties(0).multi_processor_count * ctas_per_sm
+    B = 3 * G
+    lens = [0 if G <= b < 2 * G else 1 + (37 * b) % 300 for b in range(B)]
+    x = inputs.make_inputs(B, 1, 100, 300, d, d, "key_padding", seed=5200 + d, key_lengths=lens)
+    check_full(x, f"empty middle tiles d={d}")
+
+
 @pytest.mark.parametrize("mask", ["none", "causal", "key_padding"])
 def test_large_scores_force_rescaling(mask):
     """Q and K scaled by 8: scores spread over hundreds, so the running maximum

@@ -511,7 +511,9 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 TilePos nt = t;
                 advance<MASK>(nt, u_step, p);
                 while (nt.u < p.num_units && tile_of<MASK>(nt.u, nt.ti, p).nkv == 0) advance<MASK>(nt, u_step, p);
-                if (nt.u < p.num_units) {
+                // (a tile without keys between two with keys finds its successor's Q
+                // already copied by the tile before it)
+                if (nt.u < p.num_units && !(q_done.u == nt.u && q_done.ti == nt.ti)) {
                     ok = copy_q();
                     if (!ok) break;
                     q_done = nt;
