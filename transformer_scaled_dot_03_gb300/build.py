@@ -20,7 +20,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn_sm103a.so")
 SOURCES = ["attn_api.cu", "attn_fwd_d64.cu", "attn_fwd_d128.cu", "attn_fwd_dmix.cu", "attn_fwd_alibi.cu",
            "attn_bwd_d64.cu", "attn_bwd_d128.cu", "attn_bwd_alibi.cu", "attn_bwd_dmix.cu", "attn_decode.cu", "attn_proj.cu"]
-HEADERS = ["attn_internal.h", "attn_softmax.cuh", "attn_kernel_dp.cuh", "attn_kernel_bwd.cuh", "attn_kernel_decode.cuh",
+HEADERS = ["attn_internal.h", "attn_softmax.cuh", "attn_kernel_dp.cuh", "attn_kernel_bwd.cuh", "attn_kernel_bwd128.cuh", "attn_kernel_decode.cuh",
            "attn_kernel_proj.cuh", "sm103a.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -577,10 +577,12 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
     float* dd = reinterpret_cast<float*>(wsb + ws.dd_off);
 
     attn::BwdMaps maps;
-    if ((rc = make_map(enc, &maps.q, Q, bh, n, d_k, 128)) != ATTN_OK) return rc;
+    // the d_k = d_v = 128 kernel walks the queries in 64-row steps
+    const uint32_t q_box = (d_k == 128 && d_v == 128) ? 64u : 128u;
+    if ((rc = make_map(enc, &maps.q, Q, bh, n, d_k, q_box)) != ATTN_OK) return rc;
     if ((rc = make_map(enc, &maps.k, K, bh, m, d_k, 128)) != ATTN_OK) return rc;
     if ((rc = make_map(enc, &maps.v, V, bh, m, d_v, 128)) != ATTN_OK) return rc;
-    if ((rc = make_map(enc, &maps.dout, dO, bh, n, d_v, 128)) != ATTN_OK) return rc;
+    if ((rc = make_map(enc, &maps.dout, dO, bh, n, d_v, q_box)) != ATTN_OK) return rc;
     if ((rc = make_map(enc, &maps.dk, dK, bh, m, d_k, 32)) != ATTN_OK) return rc;
     if ((rc = make_map(enc, &maps.dv, dV, bh, m, d_v, 32)) != ATTN_OK) return rc;
     if ((rc = make_map_f32(enc, &maps.dq_acc, dq_acc, bh, n, d_k)) != ATTN_OK) return rc;

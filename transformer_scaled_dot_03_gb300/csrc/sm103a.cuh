@@ -62,6 +62,40 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// A probe that may suspend the thread for up to `hint_ns` while the phase is
+// incomplete (it resumes when the phase completes): waiting warps then leave the
+// scheduler's issue slots to the warps that have work.
+__device__ __forceinline__ bool mbar_test_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+// mbar_wait with suspending probes (mbar_test_hint).
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity, volatile uint32_t* abort_word,
+                                                  uint32_t* status, uint32_t code, uint64_t limit_ns,
+                                                  uint32_t hint_ns)
+{
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_test_hint(bar, parity, hint_ns)) return true;
+        if (*abort_word) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *abort_word = 1u;
+            if (status) atomicOr(status, code);
+            return false;
+        }
+    }
+}
+
 // Bounded wait. Gives up after `limit_ns` of wall time or as soon as the CTA's
 // abort word (shared memory) is non-zero; on its own timeout it sets the abort
 // word and ORs `code` into the device status word. Returns true on success.
