@@ -956,9 +956,9 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     const int s = gt % L::QS;
                     const uint32_t parity = static_cast<uint32_t>(gt) & 1u;
                     const int q0 = (w.qb_lo + t) * BM;
-                    ok = mbar_wait(bar(L::B_QFULL + s), static_cast<uint32_t>(gt / L::QS) & 1u, abort_word, p.status,
-                                   STATUS_SOFTMAX_WAIT, limit) &&
-                         mbar_wait(bar(L::B_SFULL), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit);
+                    ok = mbar_wait_suspend(bar(L::B_QFULL + s), static_cast<uint32_t>(gt / L::QS) & 1u, abort_word, p.status,
+                                   STATUS_SOFTMAX_WAIT, limit, 2000u) &&
+                         mbar_wait_suspend(bar(L::B_SFULL), parity, abort_word, p.status, STATUS_SOFTMAX_WAIT, limit, 2000u);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
@@ -1012,8 +1012,8 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     }
                     // the previous tile's dV, dK, dQ have consumed Pᵀ and dS
                     if (gt > 0) {
-                        ok = mbar_wait(bar(L::B_BDONE), parity ^ 1u, abort_word, p.status, STATUS_SOFTMAX_WAIT,
-                                       limit);
+                        ok = mbar_wait_suspend(bar(L::B_BDONE), parity ^ 1u, abort_word, p.status, STATUS_SOFTMAX_WAIT,
+                                       limit, 2000u);
                         ok = __all_sync(0xffffffffu, ok);
                         if (!ok) break;
                         tc_fence_after();
@@ -1055,8 +1055,8 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 // overwrite them), stages them in its own dQ staging chunk (the last
                 // tile's dQ = dS K may still be reading the dS area) once its earlier
                 // reduce-adds have read it, and stores them with one TMA store.
-                ok = mbar_wait(bar(L::B_DKVDONE), static_cast<uint32_t>(it) & 1u, abort_word, p.status,
-                               STATUS_SOFTMAX_WAIT, limit);
+                ok = mbar_wait_suspend(bar(L::B_DKVDONE), static_cast<uint32_t>(it) & 1u, abort_word, p.status,
+                               STATUS_SOFTMAX_WAIT, limit, 2000u);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -1096,8 +1096,8 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         }
         if (ok && has_prev) {
             // the last tile's dQ
-            ok = mbar_wait(bar(L::B_BDONE), static_cast<uint32_t>(gt - 1) & 1u, abort_word, p.status,
-                           STATUS_SOFTMAX_WAIT, limit);
+            ok = mbar_wait_suspend(bar(L::B_BDONE), static_cast<uint32_t>(gt - 1) & 1u, abort_word, p.status,
+                           STATUS_SOFTMAX_WAIT, limit, 2000u);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) {
                 tc_fence_after();

@@ -291,7 +291,10 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             const uint64_t dK_mn = sdesc_sw128(sK, KV_CHUNK, 1024);
             const uint64_t dS_k = sdesc_sw128(sdS, 16, 1024);
             const uint64_t dS_mn = sdesc_sw128(sdS, KV_CHUNK, 1024);
+            // (a phase that has already completed is seen by a non-blocking probe,
+            // which returns sooner than a potentially suspending one)
             auto wait = [&](int b, uint32_t parity) -> bool {
+                if (__all_sync(0xffffffffu, mbar_test_now(bar(b), parity))) return true;
                 const bool r = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_MMA_WAIT, limit);
                 return __all_sync(0xffffffffu, r);
             };

@@ -405,8 +405,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // Copy a tile's Q row from shared memory (128-byte swizzle) into the
         // tensor-memory Q buffer the S MMA reads, then free the shared buffer.
         auto copy_q = [&]() -> bool {
-            bool w_ok = mbar_wait(bar(L::B_QFULL), static_cast<uint32_t>(qc) & 1u, abort_word, p.status,
-                                  STATUS_SOFTMAX_WAIT, limit);
+            bool w_ok = mbar_wait_suspend(bar(L::B_QFULL), static_cast<uint32_t>(qc) & 1u, abort_word, p.status,
+                                  STATUS_SOFTMAX_WAIT, limit, 2000u);
             w_ok = __all_sync(0xffffffffu, w_ok);
             if (!w_ok) return false;
             const uint32_t qt = tmem + lane_base + L::QT_COL + static_cast<uint32_t>(qc & 1) * (DK / 2);
@@ -447,8 +447,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
 
             for (int j = 0; j < w.nkv; ++j, ++g) {
-                ok = mbar_wait(bar(L::B_SFULL), static_cast<uint32_t>(g) & 1u, abort_word, p.status,
-                               STATUS_SOFTMAX_WAIT, limit);
+                ok = mbar_wait_suspend(bar(L::B_SFULL), static_cast<uint32_t>(g) & 1u, abort_word, p.status,
+                               STATUS_SOFTMAX_WAIT, limit, 2000u);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -471,8 +471,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 if (g > 0) {
                     // the previous O += P V must be complete: it reads the P columns,
                     // and O is rescaled below
-                    ok = mbar_wait(bar(L::B_PVDONE), static_cast<uint32_t>(g - 1) & 1u, abort_word, p.status,
-                                   STATUS_SOFTMAX_WAIT, limit);
+                    ok = mbar_wait_suspend(bar(L::B_PVDONE), static_cast<uint32_t>(g - 1) & 1u, abort_word, p.status,
+                                   STATUS_SOFTMAX_WAIT, limit, 2000u);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
@@ -498,8 +498,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
             // ---------------------------------------------- epilogue of this tile
             if (w.nkv > 0) {
-                ok = mbar_wait(bar(L::B_PVDONE), static_cast<uint32_t>(g - 1) & 1u, abort_word, p.status,
-                               STATUS_SOFTMAX_WAIT, limit);
+                ok = mbar_wait_suspend(bar(L::B_PVDONE), static_cast<uint32_t>(g - 1) & 1u, abort_word, p.status,
+                               STATUS_SOFTMAX_WAIT, limit, 2000u);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();

@@ -62,6 +62,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// A non-blocking probe of phase `parity` (mbarrier.test_wait: returns at once).
+__device__ __forceinline__ bool mbar_test_now(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // A probe that may suspend the thread for up to `hint_ns` while the phase is
 // incomplete (it resumes when the phase completes): waiting warps then leave the
 // scheduler's issue slots to the warps that have work.
