@@ -642,7 +642,16 @@ def run_launches(args):
     Q, K, V = x.Q.to(dev), x.K.to(dev), x.V.to(dev)
     lens = x.key_lengths.to(dev) if x.key_lengths is not None else None
     slopes = workload_slopes(w).to(dev) if w.alibi else None
-    for _ in range(args.launches):
+    if args.pass_ == "bwd":
+        # the forward once for O and LSE, then the backward launches
+        if slopes is not None:
+            O, L = attn.attn_fwd_alibi(Q, K, V, slopes, w.mask, lens, x.scale)
+        else:
+            O, L = attn.attn_fwd(Q, K, V, w.mask, lens, x.scale)
+        dO = inputs.make_grad_output(w.B, w.H, w.n, w.d_v, seed=100 + w.seed).to(dev)
+        for _ in range(args.launches):
+            attn.attn_bwd(Q, K, V, O, L, dO, w.mask, lens, x.scale, slopes=slopes)
+    for _ in range(args.launches if args.pass_ != "bwd" else 0):
         if w.path == "decode":
             attn.attn_decode(Q, K, V, w.mask, lens, x.scale)
         elif slopes is not None:
@@ -671,7 +680,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--launches", type=int, default=0,
-                    help="only run this many untimed forward launches on the workload (for profilers)")
+                    help="only run this many untimed launches of the pass (fwd, or bwd after one forward) "
+                         "on the workload (for profilers)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch from an ncu capture of the current kernel")
     args = ap.parse_args()
