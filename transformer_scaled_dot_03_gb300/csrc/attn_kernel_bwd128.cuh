@@ -336,25 +336,36 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     issue_A(0);
                 }
             }
+            // step gt's Q slot, whether it ends its item, and its item
+            int s = 0;
+            bool last = cur.valid && cur.t == cur.w.ns - 1;
             while (ok && cur.valid) {
-                const int s = gt % L::QS;
                 const uint32_t bcol = tmem + 128u * static_cast<uint32_t>(gt & 1);
-                const bool last = cur.t == cur.w.ns - 1;
                 // The next step's scores go to the other buffer once the step before
                 // this one has had its dQᵀ read out of it; within an item they are
                 // issued ahead of this step's products. (This step's products complete
                 // B_DQDONE's next phase, so that read-out must have been seen anyway.)
                 ok = (gt == 0 || dqfree_through(gt - 1));
+                const int s1 = s == L::QS - 1 ? 0 : s + 1;
                 if (ok && !last) {
-                    ok = wait(L::B_QFULL + (gt + 1) % L::QS, static_cast<uint32_t>((gt + 1) / L::QS) & 1u);
+                    ok = wait(L::B_QFULL + s1, static_cast<uint32_t>((gt + 1) / L::QS) & 1u);
                     if (ok) {
                         tc_fence_after();
                         issue_A(gt + 1);
                     }
                 }
+                // the next step's bookkeeping while this step's P and dS are written
+                const int item = cur.item;
+                const bool first = cur.t == 0;
+                const uint32_t acc0 = first ? 0u : 1u;
+                Cursor<MASK> nx = cur;
+                nx.next(p, num_units);
+                const bool nx_last = nx.valid && nx.t == nx.w.ns - 1;
+                const uint64_t dO_mn = sdesc_sw128(sdO + s * L::TILE_Q, Q_CHUNK, 1024);
+                const uint64_t dQ_mn = sdesc_sw128(sQ + s * L::TILE_Q, Q_CHUNK, 1024);
                 ok = ok && wait(L::B_PFULL, static_cast<uint32_t>(gt) & 1u);
                 // this item's first dV, dK overwrite the accumulators of the previous item
-                if (ok && cur.t == 0 && cur.item > 0) ok = wait(L::B_DKVFREE, static_cast<uint32_t>(cur.item - 1) & 1u);
+                if (ok && first && item > 0) ok = wait(L::B_DKVFREE, static_cast<uint32_t>(item - 1) & 1u);
                 if (!ok) break;
                 tc_fence_after();
                 // dQᵀ = Kᵀ dSᵀ into the dPᵀ columns (read by now), first, so that its
@@ -365,9 +376,6 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     mma_ss_warp(bcol + 64, dK_mn + off, dS_mn + off, ID_DQ, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_warp(bar(L::B_DQDONE));
-                const uint32_t acc0 = cur.t > 0 ? 1u : 0u;
-                const uint64_t dO_mn = sdesc_sw128(sdO + s * L::TILE_Q, Q_CHUNK, 1024);
-                const uint64_t dQ_mn = sdesc_sw128(sQ + s * L::TILE_Q, Q_CHUNK, 1024);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk) {
                     const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
@@ -381,22 +389,23 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 mma_commit_warp(bar(L::B_QEMPTY + s));
                 if (last) mma_commit_warp(bar(L::B_DKVDONE));
                 mma_commit_warp(bar(L::B_BDONE));
-                const int item = cur.item;
-                cur.next(p, num_units);
                 ++gt;
                 if (last) {
                     mma_commit_warp(bar(L::B_KVEMPTY));
-                    if (cur.valid) {
+                    if (nx.valid) {
                         // a new item: its keys replace this one's once the products above
                         // are done; its first scores go to the buffer of the step before
                         ok = dqfree_through(gt - 2) &&
                              wait(L::B_KVFULL, static_cast<uint32_t>(item + 1) & 1u) &&
-                             wait(L::B_QFULL + gt % L::QS, static_cast<uint32_t>(gt / L::QS) & 1u);
+                             wait(L::B_QFULL + s1, static_cast<uint32_t>(gt / L::QS) & 1u);
                         if (!ok) break;
                         tc_fence_after();
                         issue_A(gt);
                     }
                 }
+                cur = nx;
+                s = s1;
+                last = nx_last;
             }
             mma_commit_warp(bar(L::B_DRAIN));
             bwd::drain(bar(L::B_DRAIN), 0, 100000000ull);
