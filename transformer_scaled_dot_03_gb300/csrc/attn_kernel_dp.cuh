@@ -256,8 +256,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             auto load_K = [&](int bh, int j) -> bool {
                 const int s = kc % L::KS;
                 if (kc >= L::KS &&
-                    !mbar_wait(bar(L::B_KEMPTY + s), static_cast<uint32_t>(kc / L::KS - 1) & 1u,
-                               abort_word, p.status, STATUS_TMA_WAIT, limit))
+                    !mbar_wait_suspend(bar(L::B_KEMPTY + s), static_cast<uint32_t>(kc / L::KS - 1) & 1u,
+                               abort_word, p.status, STATUS_TMA_WAIT, limit, 2000u))
                     return false;
                 mbar_arrive_expect_tx(bar(L::B_KFULL + s), L::TILE_K);
                 for (int c = 0; c < L::CHK; ++c)
@@ -269,8 +269,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             auto load_V = [&](int bh, int j) -> bool {
                 const int s = vc % L::VS;
                 if (vc >= L::VS &&
-                    !mbar_wait(bar(L::B_VEMPTY + s), static_cast<uint32_t>(vc / L::VS - 1) & 1u,
-                               abort_word, p.status, STATUS_TMA_WAIT, limit))
+                    !mbar_wait_suspend(bar(L::B_VEMPTY + s), static_cast<uint32_t>(vc / L::VS - 1) & 1u,
+                               abort_word, p.status, STATUS_TMA_WAIT, limit, 2000u))
                     return false;
                 mbar_arrive_expect_tx(bar(L::B_VFULL + s), L::TILE_V);
                 for (int c = 0; c < L::CHV; ++c)
@@ -283,8 +283,8 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 const Unit w = tile_of<MASK>(t.u, t.ti, p);
                 if (w.nkv == 0) continue;
                 // the previous tile's Q must have left the buffer
-                if (qc > 0 && !mbar_wait(bar(L::B_QFREE), static_cast<uint32_t>(qc - 1) & 1u, abort_word,
-                                         p.status, STATUS_TMA_WAIT, limit)) {
+                if (qc > 0 && !mbar_wait_suspend(bar(L::B_QFREE), static_cast<uint32_t>(qc - 1) & 1u, abort_word,
+                                         p.status, STATUS_TMA_WAIT, limit, 2000u)) {
                     ok = false;
                     break;
                 }
@@ -317,7 +317,7 @@ attn_fwd_dp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const uint64_t dV0 = sdesc_sw128(sV, CHUNK_BYTES, 1024);
             int qc = 0, kc = 0, vc = 0, g = 0;   // g: key-tile steps over all tiles
             auto wait = [&](int b, uint32_t parity) -> bool {
-                const bool r = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_MMA_WAIT, limit);
+                const bool r = mbar_wait_suspend(bar(b), parity, abort_word, p.status, STATUS_MMA_WAIT, limit, 2000u);
                 return __all_sync(0xffffffffu, r);
             };
             auto issue_S = [&](int s) {
