@@ -15,9 +15,10 @@
 // key, the step's 64 queries contiguous), where it is the K-major A operand of
 // dK += dSᵀ Q and the MN-major B operand of dQᵀ.
 //
-// Order on the tensor pipe: the scores of step g + 1 (into the buffer of step g - 1,
-// once its dQᵀ has been read out), then the products of step g, dQᵀ first so that
-// its read-out overlaps dV and dK and the buffer frees early.
+// Two warps issue the MMAs: one every step's scores, the other every step's
+// products (dQᵀ first, so that its read-out overlaps dV and dK and the buffer frees
+// early). The scores of step g + 2 go to step g's buffer once step g's products are
+// complete and its dQᵀ has been read out.
 //
 //   warps 0-7   thread = key: Pᵀ = exp2(Sᵀ·c - LSE₂), dS = Pᵀ ∘ (dPᵀ - D) for the
 //               step's 64 queries, warp w taking tensor-memory lanes 32(w % 4)..
@@ -27,8 +28,9 @@
 //               which frees the step buffer for the step after next; thread = key
 //               for the item's dV and dK (read out, scaled, stored)
 //   warp  12    TMA producer: K and V per item, Q, dO, LSE, D per step (3 slots)
-//   warp  13    tcgen05.mma issuer, owns the tensor-memory allocation
-//   warps 14-15 idle
+//   warp  13    tcgen05.mma issuer of the scores, owns the tensor-memory allocation
+//   warp  14    tcgen05.mma issuer of the products
+//   warp  15    idle
 // Tensor memory: buffer b (b = step % 2) at columns [128b, 128b + 128): Sᵀ in
 // [128b, 128b + 64), each query half's Pᵀ (16 columns) over the first 16 of its own
 // 32 Sᵀ columns (so no warp writes columns another warp may still be reading);
@@ -64,7 +66,8 @@ struct Layout {
     static constexpr int DQ_THREADS = 128;            // warps 8-11
     static constexpr int WARP_DQ = 8;
     static constexpr int WARP_TMA = 12;
-    static constexpr int WARP_MMA = 13;
+    static constexpr int WARP_MMA = 13;               // issues the scores, owns the tensor memory
+    static constexpr int WARP_MMA_B = 14;             // issues the products
     static constexpr int QS = 3;                      // Q/dO/LSE/D ring depth
     static constexpr int TILE_KV = 2 * KV_CHUNK;      // a 128 x 128 K or V tile
     static constexpr int TILE_Q = 2 * Q_CHUNK;        // a 64 x 128 Q or dO tile
@@ -83,13 +86,13 @@ struct Layout {
     static constexpr int B_QEMPTY = B_QFULL + QS;
     static constexpr int B_SFULL = B_QEMPTY + QS;   // [2] Sᵀ, dPᵀ of a step in buffer b       (commit)
     static constexpr int B_PFULL = B_SFULL + 2;     // Pᵀ and dS of a step written              (256 arrivals)
-    static constexpr int B_DQDONE = B_PFULL + 1;    // dQᵀ of a step done                       (commit)
-    static constexpr int B_BDONE = B_DQDONE + 1;    // dV, dK of a step done (dS read)          (commit)
-    static constexpr int B_DQFREE = B_BDONE + 1;    // a step's dQᵀ read out of tensor memory  (128 arrivals)
-    static constexpr int B_DKVDONE = B_DQFREE + 1;  // an item's dV, dK complete                (commit)
+    static constexpr int B_DQDONE = B_PFULL + 1;    // [2] dQᵀ of a step in buffer b done       (commit)
+    static constexpr int B_BDONE = B_DQDONE + 2;    // [2] all products of a step in buffer b   (commit)
+    static constexpr int B_DQFREE = B_BDONE + 2;    // [2] dQᵀ of buffer b read out             (128 arrivals)
+    static constexpr int B_DKVDONE = B_DQFREE + 2;  // an item's dV, dK complete                (commit)
     static constexpr int B_DKVFREE = B_DKVDONE + 1; // an item's dV, dK read out                (128 arrivals)
-    static constexpr int B_DRAIN = B_DKVFREE + 1;
-    static constexpr int B_NEVER = B_DRAIN + 1;
+    static constexpr int B_DRAIN = B_DKVFREE + 1;   // [2] each issuing warp's last MMAs done
+    static constexpr int B_NEVER = B_DRAIN + 2;
     static constexpr int NBARS = B_NEVER + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16 + 1024;
@@ -199,12 +202,14 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         mbar_init(bar(L::B_SFULL), 1);
         mbar_init(bar(L::B_SFULL + 1), 1);
         mbar_init(bar(L::B_PFULL), L::COMPUTE_THREADS);
-        mbar_init(bar(L::B_DQDONE), 1);
-        mbar_init(bar(L::B_BDONE), 1);
-        mbar_init(bar(L::B_DQFREE), L::DQ_THREADS);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::B_DQDONE + b), 1);
+            mbar_init(bar(L::B_BDONE + b), 1);
+            mbar_init(bar(L::B_DQFREE + b), L::DQ_THREADS);
+            mbar_init(bar(L::B_DRAIN + b), 1);
+        }
         mbar_init(bar(L::B_DKVDONE), 1);
         mbar_init(bar(L::B_DKVFREE), L::DQ_THREADS);
-        mbar_init(bar(L::B_DRAIN), 1);
         mbar_init(bar(L::B_NEVER), 1);
         *abort_word = 0u;
         fence_mbar_init();
@@ -281,8 +286,13 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             if (kv_issued > 0) bwd::drain(bar(L::B_KVFULL), static_cast<uint32_t>(kv_issued - 1) & 1u, 100000000ull);
             for (int i = gt - 1; i >= 0 && i >= gt - L::QS; --i)
                 bwd::drain(bar(L::B_QFULL + i % L::QS), static_cast<uint32_t>(i / L::QS) & 1u, 100000000ull);
-        } else if (warp == L::WARP_MMA) {
-            // ================================================== MMA issuer (whole warp, one elected lane)
+        } else if (warp == L::WARP_MMA || warp == L::WARP_MMA_B) {
+            // ================================================== MMA issuers (whole warp, one elected lane)
+            // Warp 13 issues every step's scores, warp 14 every step's products, so
+            // that one warp's bookkeeping and waits overlap the other's issue. Issue
+            // order between the two is not an order on the tensor pipe: step h's
+            // scores go to the buffer of step h - 2 only once that step's products
+            // are complete (B_BDONE) and its dQᵀ has been read out (B_DQFREE).
             constexpr uint32_t ID_S = idesc_bf16_f32(BK, BQ, false, false);   // M = keys, N = queries
             constexpr uint32_t ID_KV = idesc_bf16_f32(BK, D, false, true);    // M = keys, N = head dims
             constexpr uint32_t ID_DQ = idesc_bf16_f32(D, BQ, true, true);     // M = head dims, N = queries
@@ -298,117 +308,83 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 const bool r = mbar_wait(bar(b), parity, abort_word, p.status, STATUS_MMA_WAIT, limit);
                 return __all_sync(0xffffffffu, r);
             };
-            // Sᵀ = K Qᵀ and dPᵀ = V dOᵀ of step h into buffer h % 2, the two accumulation
-            // chains interleaved
-            auto issue_A = [&](int h) {
-                const int qs = h % L::QS;
-                const uint64_t dQ_k = sdesc_sw128(sQ + qs * L::TILE_Q, 16, 1024);
-                const uint64_t dO_k = sdesc_sw128(sdO + qs * L::TILE_Q, 16, 1024);
-                const uint32_t col = tmem + 128u * static_cast<uint32_t>(h & 1);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t aoff = static_cast<uint64_t>(((kk / 4) * KV_CHUNK + (kk % 4) * 32) >> 4);
-                    const uint64_t boff = static_cast<uint64_t>(((kk / 4) * Q_CHUNK + (kk % 4) * 32) >> 4);
-                    mma_ss_warp(col, dK_k + aoff, dQ_k + boff, ID_S, kk > 0 ? 1u : 0u);
-                    mma_ss_warp(col + 64, dV_k + aoff, dO_k + boff, ID_S, kk > 0 ? 1u : 0u);
-                }
-                mma_commit_warp(bar(L::B_SFULL + (h & 1)));
-            };
-            // B_DQFREE phases are consumed in step order; step dqf's is the next. A
-            // step's products complete B_DQDONE's next phase, so the read-out of the step
-            // before must have been seen first.
-            int dqf = 0;
-            auto dqfree_through = [&](int h) -> bool {
-                while (dqf <= h) {
-                    if (!wait(L::B_DQFREE, static_cast<uint32_t>(dqf) & 1u)) return false;
-                    ++dqf;
-                }
-                return true;
-            };
             Cursor<MASK> cur;
             cur.start(p, num_units);
             bool ok = true;
-            int gt = 0;
-            if (cur.valid) {
-                ok = wait(L::B_KVFULL, 0) && wait(L::B_QFULL, 0);
-                if (ok) {
+            int g = 0;      // step
+            int s = 0;      // its Q slot
+            if (warp == L::WARP_MMA) {
+                while (ok && cur.valid) {
+                    const int b = g & 1;
+                    const uint32_t rp = static_cast<uint32_t>((g - 2) >> 1) & 1u;   // step g - 2's phase
+                    ok = (g < 2 || (wait(L::B_BDONE + b, rp) && wait(L::B_DQFREE + b, rp))) &&
+                         // an item's keys (loaded once the previous item's products are done)
+                         (cur.t != 0 || wait(L::B_KVFULL, static_cast<uint32_t>(cur.item) & 1u)) &&
+                         wait(L::B_QFULL + s, static_cast<uint32_t>(g / L::QS) & 1u);
+                    if (!ok) break;
                     tc_fence_after();
-                    issue_A(0);
+                    // Sᵀ = K Qᵀ and dPᵀ = V dOᵀ into buffer b, the two chains interleaved
+                    const uint64_t dQ_k = sdesc_sw128(sQ + s * L::TILE_Q, 16, 1024);
+                    const uint64_t dO_k = sdesc_sw128(sdO + s * L::TILE_Q, 16, 1024);
+                    const uint32_t col = tmem + 128u * static_cast<uint32_t>(b);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t aoff = static_cast<uint64_t>(((kk / 4) * KV_CHUNK + (kk % 4) * 32) >> 4);
+                        const uint64_t boff = static_cast<uint64_t>(((kk / 4) * Q_CHUNK + (kk % 4) * 32) >> 4);
+                        mma_ss_warp(col, dK_k + aoff, dQ_k + boff, ID_S, kk > 0 ? 1u : 0u);
+                        mma_ss_warp(col + 64, dV_k + aoff, dO_k + boff, ID_S, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit_warp(bar(L::B_SFULL + b));
+                    ++g;
+                    s = s == L::QS - 1 ? 0 : s + 1;
+                    cur.next(p, num_units);
+                }
+            } else {
+                while (ok && cur.valid) {
+                    const int b = g & 1;
+                    const uint32_t bcol = tmem + 128u * static_cast<uint32_t>(b);
+                    const bool last = cur.t == cur.w.ns - 1;
+                    const int item = cur.item;
+                    const uint32_t acc0 = cur.t > 0 ? 1u : 0u;
+                    const uint64_t dO_mn = sdesc_sw128(sdO + s * L::TILE_Q, Q_CHUNK, 1024);
+                    const uint64_t dQ_mn = sdesc_sw128(sQ + s * L::TILE_Q, Q_CHUNK, 1024);
+                    ok = wait(L::B_PFULL, static_cast<uint32_t>(g) & 1u);
+                    // this item's first dV, dK overwrite the accumulators of the previous item
+                    if (ok && cur.t == 0 && item > 0) ok = wait(L::B_DKVFREE, static_cast<uint32_t>(item - 1) & 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // dQᵀ = Kᵀ dSᵀ into the dPᵀ columns (read by now), first, so that its
+                    // read-out overlaps dV and dK
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
+                        mma_ss_warp(bcol + 64, dK_mn + off, dS_mn + off, ID_DQ, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit_warp(bar(L::B_DQDONE + b));
+#pragma unroll
+                    for (int kk = 0; kk < BQ / 16; ++kk) {
+                        const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
+                        // Pᵀ of queries 16kk.. : the query half kk / 2, its (kk % 2)-th 8 columns
+                        mma_ts_warp(tmem + L::DV_COL, bcol + (kk >> 1) * 32 + (kk & 1) * 8, dO_mn + off, ID_KV,
+                                    (acc0 | kk) ? 1u : 0u);
+                        mma_ss_warp(tmem + L::DK_COL, dS_k + static_cast<uint64_t>((kk * 32) >> 4), dQ_mn + off,
+                                    ID_KV, (acc0 | kk) ? 1u : 0u);
+                    }
+                    // the last reads of this step's Q and dO are issued
+                    mma_commit_warp(bar(L::B_QEMPTY + s));
+                    if (last) mma_commit_warp(bar(L::B_DKVDONE));
+                    mma_commit_warp(bar(L::B_BDONE + b));
+                    // an item's keys are read for the last time by its last products
+                    // (its last scores are complete: their P came before)
+                    if (last) mma_commit_warp(bar(L::B_KVEMPTY));
+                    ++g;
+                    s = s == L::QS - 1 ? 0 : s + 1;
+                    cur.next(p, num_units);
                 }
             }
-            // step gt's Q slot, whether it ends its item, and its item
-            int s = 0;
-            bool last = cur.valid && cur.t == cur.w.ns - 1;
-            while (ok && cur.valid) {
-                const uint32_t bcol = tmem + 128u * static_cast<uint32_t>(gt & 1);
-                // The next step's scores go to the other buffer once the step before
-                // this one has had its dQᵀ read out of it; within an item they are
-                // issued ahead of this step's products. (This step's products complete
-                // B_DQDONE's next phase, so that read-out must have been seen anyway.)
-                ok = (gt == 0 || dqfree_through(gt - 1));
-                const int s1 = s == L::QS - 1 ? 0 : s + 1;
-                if (ok && !last) {
-                    ok = wait(L::B_QFULL + s1, static_cast<uint32_t>((gt + 1) / L::QS) & 1u);
-                    if (ok) {
-                        tc_fence_after();
-                        issue_A(gt + 1);
-                    }
-                }
-                // the next step's bookkeeping while this step's P and dS are written
-                const int item = cur.item;
-                const bool first = cur.t == 0;
-                const uint32_t acc0 = first ? 0u : 1u;
-                Cursor<MASK> nx = cur;
-                nx.next(p, num_units);
-                const bool nx_last = nx.valid && nx.t == nx.w.ns - 1;
-                const uint64_t dO_mn = sdesc_sw128(sdO + s * L::TILE_Q, Q_CHUNK, 1024);
-                const uint64_t dQ_mn = sdesc_sw128(sQ + s * L::TILE_Q, Q_CHUNK, 1024);
-                ok = ok && wait(L::B_PFULL, static_cast<uint32_t>(gt) & 1u);
-                // this item's first dV, dK overwrite the accumulators of the previous item
-                if (ok && first && item > 0) ok = wait(L::B_DKVFREE, static_cast<uint32_t>(item - 1) & 1u);
-                if (!ok) break;
-                tc_fence_after();
-                // dQᵀ = Kᵀ dSᵀ into the dPᵀ columns (read by now), first, so that its
-                // read-out overlaps dV and dK
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
-                    mma_ss_warp(bcol + 64, dK_mn + off, dS_mn + off, ID_DQ, kk > 0 ? 1u : 0u);
-                }
-                mma_commit_warp(bar(L::B_DQDONE));
-#pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
-                    // Pᵀ of queries 16kk.. : the query half kk / 2, its (kk % 2)-th 8 columns
-                    mma_ts_warp(tmem + L::DV_COL, bcol + (kk >> 1) * 32 + (kk & 1) * 8, dO_mn + off, ID_KV,
-                                (acc0 | kk) ? 1u : 0u);
-                    mma_ss_warp(tmem + L::DK_COL, dS_k + static_cast<uint64_t>((kk * 32) >> 4), dQ_mn + off, ID_KV,
-                                (acc0 | kk) ? 1u : 0u);
-                }
-                // the last reads of this step's Q and dO are issued
-                mma_commit_warp(bar(L::B_QEMPTY + s));
-                if (last) mma_commit_warp(bar(L::B_DKVDONE));
-                mma_commit_warp(bar(L::B_BDONE));
-                ++gt;
-                if (last) {
-                    mma_commit_warp(bar(L::B_KVEMPTY));
-                    if (nx.valid) {
-                        // a new item: its keys replace this one's once the products above
-                        // are done; its first scores go to the buffer of the step before
-                        ok = dqfree_through(gt - 2) &&
-                             wait(L::B_KVFULL, static_cast<uint32_t>(item + 1) & 1u) &&
-                             wait(L::B_QFULL + s1, static_cast<uint32_t>(gt / L::QS) & 1u);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_A(gt);
-                    }
-                }
-                cur = nx;
-                s = s1;
-                last = nx_last;
-            }
-            mma_commit_warp(bar(L::B_DRAIN));
-            bwd::drain(bar(L::B_DRAIN), 0, 100000000ull);
+            const int dr = warp == L::WARP_MMA ? 0 : 1;
+            mma_commit_warp(bar(L::B_DRAIN + dr));
+            bwd::drain(bar(L::B_DRAIN + dr), 0, 100000000ull);
         }
         __syncwarp();
     } else if (warp >= L::WARP_DQ) {
@@ -441,7 +417,7 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 }
                 for (int t = 0; ok && t < w.ns; ++t) {
                     const int q0 = (w.s_lo + t) * BQ;
-                    ok = mbar_wait_suspend(bar(L::B_DQDONE), static_cast<uint32_t>(gt) & 1u, abort_word, p.status,
+                    ok = mbar_wait_suspend(bar(L::B_DQDONE + (gt & 1)), static_cast<uint32_t>(gt >> 1) & 1u, abort_word, p.status,
                                    STATUS_SOFTMAX_WAIT, limit, kWaitHintNs);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
@@ -453,7 +429,7 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     tmem_ld32(tmem + lane_base + col + 32, a + 32);
                     tmem_wait_ld();
                     tc_fence_before();
-                    mbar_arrive(bar(L::B_DQFREE));
+                    mbar_arrive(bar(L::B_DQFREE + (gt & 1)));
                     // the reduce-adds of the previous step must have read the staging blocks
                     if (bulk_pending && lane == 0) bulk_wait_group_read0();
                     __syncwarp();
@@ -598,7 +574,7 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     }
                     // the previous step's dQᵀ, dV and dK have read dS (B_BDONE follows them)
                     if (gt > 0) {
-                        ok = mbar_wait_suspend(bar(L::B_BDONE), static_cast<uint32_t>(gt - 1) & 1u, abort_word, p.status,
+                        ok = mbar_wait_suspend(bar(L::B_BDONE + ((gt - 1) & 1)), static_cast<uint32_t>((gt - 1) >> 1) & 1u, abort_word, p.status,
                                        STATUS_SOFTMAX_WAIT, limit, kWaitHintNs);
                         ok = __all_sync(0xffffffffu, ok);
                         if (!ok) break;
