@@ -131,10 +131,12 @@ def test_bwd_long_d128_small_batch():
 @pytest.mark.parametrize("mask,B,H,n,m,lens", [
     ("causal", 3, 64, 256, 256, None),
     ("key_padding", 4, 40, 200, 300, [300, 129, 0, 64]),
+    ("none", 3, 64, 64, 256, None),
 ])
 def test_bwd_d128_many_items_per_cta(mask, B, H, n, m, lens):
     """More work items (128-key tiles) than SMs at d = 128, so that the persistent
-    CTAs move from one item to the next (new keys, dV and dK read out and restarted)."""
+    CTAs move from one item to the next (new keys, dV and dK read out and restarted);
+    with n = 64 every item is a single 64-query step."""
     x, dO = case(B, H, n, m, 128, mask, seed=8600 + n + H, lens=lens)
     check_bwd(x, dO, f"d128 items {mask}")
 

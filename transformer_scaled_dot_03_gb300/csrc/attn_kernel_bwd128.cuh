@@ -17,8 +17,8 @@
 //
 // Two warps issue the MMAs: one every step's scores, the other every step's
 // products (dQᵀ first, so that its read-out overlaps dV and dK and the buffer frees
-// early). The scores of step g + 2 go to step g's buffer once step g's products are
-// complete and its dQᵀ has been read out.
+// early, then dV, then dK). The scores of step g + 2 go to step g's buffer once step
+// g's dQᵀ and dV are complete and its dQᵀ has been read out.
 //
 //   warps 0-7   thread = key: Pᵀ = exp2(Sᵀ·c - LSE₂), dS = Pᵀ ∘ (dPᵀ - D) for the
 //               step's 64 queries, warp w taking tensor-memory lanes 32(w % 4)..
@@ -88,7 +88,8 @@ struct Layout {
     static constexpr int B_PFULL = B_SFULL + 2;     // Pᵀ and dS of a step written              (256 arrivals)
     static constexpr int B_DQDONE = B_PFULL + 1;    // [2] dQᵀ of a step in buffer b done       (commit)
     static constexpr int B_BDONE = B_DQDONE + 2;    // [2] all products of a step in buffer b   (commit)
-    static constexpr int B_DQFREE = B_BDONE + 2;    // [2] dQᵀ of buffer b read out             (128 arrivals)
+    static constexpr int B_PUSED = B_BDONE + 2;     // [2] Pᵀ of buffer b consumed (dQᵀ, dV)    (commit)
+    static constexpr int B_DQFREE = B_PUSED + 2;    // [2] dQᵀ of buffer b read out             (128 arrivals)
     static constexpr int B_DKVDONE = B_DQFREE + 2;  // an item's dV, dK complete                (commit)
     static constexpr int B_DKVFREE = B_DKVDONE + 1; // an item's dV, dK read out                (128 arrivals)
     static constexpr int B_DRAIN = B_DKVFREE + 1;   // [2] each issuing warp's last MMAs done
@@ -205,6 +206,7 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(L::B_DQDONE + b), 1);
             mbar_init(bar(L::B_BDONE + b), 1);
+            mbar_init(bar(L::B_PUSED + b), 1);
             mbar_init(bar(L::B_DQFREE + b), L::DQ_THREADS);
             mbar_init(bar(L::B_DRAIN + b), 1);
         }
@@ -291,8 +293,9 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             // Warp 13 issues every step's scores, warp 14 every step's products, so
             // that one warp's bookkeeping and waits overlap the other's issue. Issue
             // order between the two is not an order on the tensor pipe: step h's
-            // scores go to the buffer of step h - 2 only once that step's products
-            // are complete (B_BDONE) and its dQᵀ has been read out (B_DQFREE).
+            // scores go to the buffer of step h - 2 only once that step's dQᵀ and dV
+            // (the products that use the buffer) are complete (B_PUSED) and its dQᵀ
+            // has been read out (B_DQFREE).
             constexpr uint32_t ID_S = idesc_bf16_f32(BK, BQ, false, false);   // M = keys, N = queries
             constexpr uint32_t ID_KV = idesc_bf16_f32(BK, D, false, true);    // M = keys, N = head dims
             constexpr uint32_t ID_DQ = idesc_bf16_f32(D, BQ, true, true);     // M = head dims, N = queries
@@ -317,7 +320,7 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 while (ok && cur.valid) {
                     const int b = g & 1;
                     const uint32_t rp = static_cast<uint32_t>((g - 2) >> 1) & 1u;   // step g - 2's phase
-                    ok = (g < 2 || (wait(L::B_BDONE + b, rp) && wait(L::B_DQFREE + b, rp))) &&
+                    ok = (g < 2 || (wait(L::B_PUSED + b, rp) && wait(L::B_DQFREE + b, rp))) &&
                          // an item's keys (loaded once the previous item's products are done)
                          (cur.t != 0 || wait(L::B_KVFULL, static_cast<uint32_t>(cur.item) & 1u)) &&
                          wait(L::B_QFULL + s, static_cast<uint32_t>(g / L::QS) & 1u);
@@ -361,12 +364,19 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                         mma_ss_warp(bcol + 64, dK_mn + off, dS_mn + off, ID_DQ, kk > 0 ? 1u : 0u);
                     }
                     mma_commit_warp(bar(L::B_DQDONE + b));
+                    // dV += Pᵀ dO, the last product that uses the step's buffer
 #pragma unroll
                     for (int kk = 0; kk < BQ / 16; ++kk) {
                         const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
                         // Pᵀ of queries 16kk.. : the query half kk / 2, its (kk % 2)-th 8 columns
                         mma_ts_warp(tmem + L::DV_COL, bcol + (kk >> 1) * 32 + (kk & 1) * 8, dO_mn + off, ID_KV,
                                     (acc0 | kk) ? 1u : 0u);
+                    }
+                    mma_commit_warp(bar(L::B_PUSED + b));
+                    // dK += dSᵀ Q (shared memory only)
+#pragma unroll
+                    for (int kk = 0; kk < BQ / 16; ++kk) {
+                        const uint64_t off = static_cast<uint64_t>((kk * 2048) >> 4);
                         mma_ss_warp(tmem + L::DK_COL, dS_k + static_cast<uint64_t>((kk * 32) >> 4), dQ_mn + off,
                                     ID_KV, (acc0 | kk) ? 1u : 0u);
                     }
