@@ -50,8 +50,9 @@ def test_forced_timeout_reports_and_recovers(mask, d):
 
 @pytest.mark.parametrize("d", [64, 128])
 def test_forced_timeout_in_the_backward(d):
-    """The same for the backward kernels (the persistent pipelined one at d = 64, the
-    generic one at d = 128): the forced wait gives up, the status reports it, and a
+    """The same for the backward kernels (the persistent 128-query-tile kernel at
+    d = 64, the 64-query-step kernel with two MMA issuers and a read-out warpgroup at
+    d = 128): the forced wait gives up, the status reports it, every role leaves, and a
     normal backward afterwards matches the oracle."""
     x = inputs.make_inputs(2, 2, 260, 260, d, d, "causal", seed=5100 + d)
     dO = inputs.make_grad_output(2, 2, 260, d, seed=5101 + d)
