@@ -531,8 +531,8 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 //     Sᵀ, dPᵀ (next)  as soon as the softmax warps have loaded Sᵀ, dPᵀ (t)
 //     dV, dK, dQ (t)  once Pᵀ (t) and dS (t) are written,
 // so the tensor cores compute the next tile's scores while the softmax warps turn
-// tile t's into Pᵀ and dS. The dQ of a tile is read out one iteration later,
-// through a staging area of its own.
+// tile t's into Pᵀ and dS (warp 10 issues the scores, warp 9 the products). The dQ
+// of a tile is read out one iteration later, through a staging area of its own.
 //
 // Persistent: one CTA per SM walks work items (b, h, 128-key tile) round-robin;
 // under the causal masks a unit pairs key tile k with key tile nkb-1-k of the same
@@ -546,10 +546,11 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 struct LayoutPipe {
     static constexpr int D = 64;
     static constexpr int TILE = CHUNK_BYTES;                 // a 128 x 64 bf16 tile
-    static constexpr int NUM_THREADS = 320;
+    static constexpr int NUM_THREADS = 352;
     static constexpr int COMPUTE_THREADS = 256;
     static constexpr int WARP_TMA = 8;
-    static constexpr int WARP_MMA = 9;
+    static constexpr int WARP_MMA = 9;                       // issues the products, owns the tensor memory
+    static constexpr int WARP_MMA_S = 10;                    // issues the scores
     static constexpr int QS = 2;                             // Q/dO/LSE/D ring depth
     static constexpr int KVS = 2;                            // K/V buffers
     static constexpr int K_OFF = 0;
@@ -572,8 +573,8 @@ struct LayoutPipe {
     static constexpr int B_DQFREE = B_BDONE + 1;    // dQ read out of tensor memory      (256 arrivals)
     static constexpr int B_DKVDONE = B_DQFREE + 1;  // an item's dV, dK complete         (commit)
     static constexpr int B_DKVFREE = B_DKVDONE + 1; // an item's dV, dK read out         (256 arrivals)
-    static constexpr int B_DRAIN = B_DKVFREE + 1;
-    static constexpr int B_NEVER = B_DRAIN + 1;
+    static constexpr int B_DRAIN = B_DKVFREE + 1;   // [2] each issuing warp's last MMAs done
+    static constexpr int B_NEVER = B_DRAIN + 2;
     static constexpr int NBARS = B_NEVER + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int BYTES = MISC_OFF + 16 + 1024;
@@ -700,6 +701,7 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         mbar_init(bar(L::B_DKVDONE), 1);
         mbar_init(bar(L::B_DKVFREE), L::COMPUTE_THREADS);
         mbar_init(bar(L::B_DRAIN), 1);
+        mbar_init(bar(L::B_DRAIN + 1), 1);
         mbar_init(bar(L::B_NEVER), 1);
         *abort_word = 0u;
         fence_mbar_init();
@@ -775,8 +777,12 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 drain(bar(L::B_KVFULL + i % L::KVS), static_cast<uint32_t>(i / L::KVS) & 1u, 100000000ull);
             for (int i = gt - 1; i >= 0 && i >= gt - L::QS; --i)
                 drain(bar(L::B_QFULL + i % L::QS), static_cast<uint32_t>(i / L::QS) & 1u, 100000000ull);
-        } else if (warp == L::WARP_MMA) {
-            // ================================================== MMA issuer (whole warp, one elected lane)
+        } else if (warp == L::WARP_MMA || warp == L::WARP_MMA_S) {
+            // ================================================== MMA issuers (whole warp, one elected lane)
+            // Warp 10 issues each tile's scores as soon as the softmax warps hold the
+            // previous tile's; warp 9 issues the products. Their MMAs touch disjoint
+            // tensor-memory columns, and every dependence between them passes through
+            // the softmax warps' barriers (B_RDONE, B_PFULL).
             constexpr uint32_t ID_S = idesc_bf16_f32(BN, BM, false, false);   // M = keys, N = queries
             constexpr uint32_t ID_KV = idesc_bf16_f32(BN, D, false, true);    // M = keys, N = d
             constexpr uint32_t ID_DQ = idesc_bf16_f32(BM, D, true, true);     // M = queries, N = d
@@ -808,30 +814,38 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             cur.start(p, num_units);
             bool ok = true;
             int gt = 0, it = 0;
-            if (cur.valid) {
-                ok = wait(L::B_KVFULL, 0) && wait(L::B_QFULL, 0);
-                if (ok) {
-                    tc_fence_after();
-                    issue_A(0, 0);
+            if (warp == L::WARP_MMA_S) {
+                if (cur.valid) {
+                    ok = wait(L::B_KVFULL, 0) && wait(L::B_QFULL, 0);
+                    if (ok) {
+                        tc_fence_after();
+                        issue_A(0, 0);
+                    }
                 }
-            }
-            while (ok && cur.valid) {
-                const int s = gt % L::QS;
-                const int ks = it % L::KVS;
-                const uint32_t parity = static_cast<uint32_t>(gt) & 1u;
-                BwdCursor<MASK> nx = cur;
-                nx.next(p, num_units);
-                if (nx.valid) {
+                while (ok && cur.valid) {
+                    BwdCursor<MASK> nx = cur;
+                    nx.next(p, num_units);
+                    if (!nx.valid) break;
                     // the next tile's scores as soon as the softmax warps hold this tile's
                     const bool new_item = nx.t == 0;
                     const int nks = (it + (new_item ? 1 : 0)) % L::KVS;
                     ok = wait(L::B_QFULL + (gt + 1) % L::QS, static_cast<uint32_t>((gt + 1) / L::QS) & 1u) &&
                          (!new_item || wait(L::B_KVFULL + nks, static_cast<uint32_t>((it + 1) / L::KVS) & 1u)) &&
-                         wait(L::B_RDONE, parity);
+                         wait(L::B_RDONE, static_cast<uint32_t>(gt) & 1u);
                     if (!ok) break;
                     tc_fence_after();
                     issue_A((gt + 1) % L::QS, nks);
+                    if (new_item) ++it;
+                    ++gt;
+                    cur = nx;
                 }
+                mma_commit_warp(bar(L::B_DRAIN + 1));
+                drain(bar(L::B_DRAIN + 1), 0, 100000000ull);
+            }
+            while (warp == L::WARP_MMA && ok && cur.valid) {
+                const int s = gt % L::QS;
+                const int ks = it % L::KVS;
+                const uint32_t parity = static_cast<uint32_t>(gt) & 1u;
                 ok = wait(L::B_PFULL, parity);
                 // this item's first dV, dK overwrite the accumulators of the previous item
                 if (ok && cur.t == 0 && it > 0) ok = wait(L::B_DKVFREE, static_cast<uint32_t>(it - 1) & 1u);
@@ -876,10 +890,12 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     ++it;
                 }
                 ++gt;
-                cur = nx;
+                cur.next(p, num_units);
             }
-            mma_commit_warp(bar(L::B_DRAIN));
-            drain(bar(L::B_DRAIN), 0, 100000000ull);
+            if (warp == L::WARP_MMA) {
+                mma_commit_warp(bar(L::B_DRAIN));
+                drain(bar(L::B_DRAIN), 0, 100000000ull);
+            }
         }
         __syncwarp();
     } else {
