@@ -738,8 +738,10 @@ int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n
     int num_sms = 0;
     int rc0 = sm_count(&num_sms);
     if (rc0 != ATTN_OK) return rc0;
-    const int64_t slots = static_cast<int64_t>(num_sms) * (d_k == 64 && d_v == 64 ? 2 : 1);
-    if (n > kDecodeMaxRows || bh >= kDecodeTileWaves * slots) {
+    // the forward kernel's CTA slots decide the path; the split kernel runs two CTAs per SM
+    const int64_t tile_slots = static_cast<int64_t>(num_sms) * (d_k == 64 && d_v == 64 ? 2 : 1);
+    const int64_t slots = static_cast<int64_t>(num_sms) * 2;
+    if (n > kDecodeMaxRows || bh >= kDecodeTileWaves * tile_slots) {
         // More rows than the split kernel holds, or enough (b, h) pairs to fill
         // every SM several times over: the tensor-core forward kernel streams each
         // pair's K and V once at the memory system's rate (its 128-row query tile

@@ -52,10 +52,12 @@ struct Layout {
     static constexpr int TILE_K = CHK * CHUNK_BYTES;        // 128 keys x DK
     static constexpr int TILE_V = CHV * CHUNK_BYTES;        // 128 keys x DV
     static constexpr bool SMALL = DK == 64 && DV == 64;
-    static constexpr int STAGES = SMALL ? 3 : 2;
+    // Two CTAs per SM at every head dim: with d = 128 a 128-key stage is 64 KB, so
+    // each CTA holds one (the two CTAs' loads and consumers interleave)
+    static constexpr int STAGES = SMALL ? 3 : 1;
     static constexpr int NUM_THREADS = 160;
     static constexpr int WARP_TMA = 4;
-    static constexpr int CTAS_PER_SM = SMALL ? 2 : 1;
+    static constexpr int CTAS_PER_SM = 2;
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + STAGES * TILE_K;
     static constexpr int Q_OFF = V_OFF + STAGES * TILE_V;    // fp32 [NQ_MAX][DK]
