@@ -738,9 +738,9 @@ int decode_impl(const void* Q, const void* K, const void* V, int B, int H, int n
     int num_sms = 0;
     int rc0 = sm_count(&num_sms);
     if (rc0 != ATTN_OK) return rc0;
-    // the forward kernel's CTA slots decide the path; the split kernel runs two CTAs per SM
+    // the forward kernel's CTA slots decide the path; the split kernel's size the chunks
     const int64_t tile_slots = static_cast<int64_t>(num_sms) * (d_k == 64 && d_v == 64 ? 2 : 1);
-    const int64_t slots = static_cast<int64_t>(num_sms) * 2;
+    const int64_t slots = static_cast<int64_t>(num_sms) * attn::decode_ctas_per_sm(d_k, d_v, decode_rows(n));
     if (n > kDecodeMaxRows || bh >= kDecodeTileWaves * tile_slots) {
         // More rows than the split kernel holds, or enough (b, h) pairs to fill
         // every SM several times over: the tensor-core forward kernel streams each

@@ -109,6 +109,13 @@ cudaError_t launch_bwd_dmix(int d_k, int d_v, int mask, const BwdMaps& maps, con
 cudaError_t launch_bwd_alibi(int d_k, int d_v, int mask, const BwdMaps& maps, const BwdParams& p, cudaStream_t stream);
 
 // Few-row forward (attn_kernel_decode.cuh): one CTA per (b, h, key chunk).
+// CTAs per SM of its kernel: three at d_k = 128 with one or two query rows (the
+// merge area then shares the key stage; the kernel fits 136 registers), else two.
+__host__ __device__ constexpr int decode_ctas_per_sm(int d_k, int d_v, int rows)
+{
+    return (d_k == 64 && d_v == 64) ? 2 : (d_k == 128 && rows <= 2 ? 3 : 2);
+}
+
 struct DecodeParams {
     const uint16_t* Q;            // bf16 [B,H,n,d_k]
     int B, H, n, m;

@@ -44,26 +44,30 @@ constexpr int NQ_MAX = 8;
 constexpr float LN2 = 0.693147180559945309f;
 constexpr float LOG2E = 1.44269504088896341f;
 
-// DK: query/key head dim, DV: value head dim.
-template <int DK, int DV>
+// DK: query/key head dim, DV: value head dim, CTAS: CTAs per SM.
+template <int DK, int DV, int CTAS>
 struct Layout {
     static constexpr int CHK = DK / 64;
     static constexpr int CHV = DV / 64;
     static constexpr int TILE_K = CHK * CHUNK_BYTES;        // 128 keys x DK
     static constexpr int TILE_V = CHV * CHUNK_BYTES;        // 128 keys x DV
     static constexpr bool SMALL = DK == 64 && DV == 64;
-    // Two CTAs per SM at every head dim: with d = 128 a 128-key stage is 64 KB, so
-    // each CTA holds one (the two CTAs' loads and consumers interleave)
+    // Two or three CTAs per SM: with d = 128 a 128-key stage is 64 KB, so each CTA
+    // holds one (the CTAs' loads and consumers interleave). At three the merge area
+    // shares the key stage, which no copy writes once the last tile is consumed.
     static constexpr int STAGES = SMALL ? 3 : 1;
     static constexpr int NUM_THREADS = 160;
     static constexpr int WARP_TMA = 4;
-    static constexpr int CTAS_PER_SM = 2;
+    static constexpr int CTAS_PER_SM = CTAS;
+    static constexpr bool RED_IN_STAGE = CTAS == 3;
     static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + STAGES * TILE_K;
     static constexpr int Q_OFF = V_OFF + STAGES * TILE_V;    // fp32 [NQ_MAX][DK]
-    static constexpr int RED_OFF = Q_OFF + NQ_MAX * DK * 4;  // per warp: m, l [NQ_MAX] then O [NQ_MAX][DV]
     static constexpr int RED_WARP = (2 * NQ_MAX + NQ_MAX * DV) * 4;
-    static constexpr int BAR_OFF = RED_OFF + 4 * RED_WARP;
+    // per warp: m, l [NQ_MAX] then O [NQ_MAX][DV]
+    static constexpr int RED_OFF = RED_IN_STAGE ? K_OFF : Q_OFF + NQ_MAX * DK * 4;
+    static constexpr int BAR_OFF = RED_IN_STAGE ? Q_OFF + NQ_MAX * DK * 4 : RED_OFF + 4 * RED_WARP;
+    static_assert(!RED_IN_STAGE || 4 * RED_WARP <= STAGES * TILE_K, "merge area inside the key stage");
     static constexpr int B_FULL = 0;
     static constexpr int B_EMPTY = STAGES;
     static constexpr int B_NEVER = 2 * STAGES;               // debug: completed by nothing
@@ -85,11 +89,12 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col)
 }
 
 template <int DK, int DV, int NQ>
-__global__ void __launch_bounds__(Layout<DK, DV>::NUM_THREADS, Layout<DK, DV>::CTAS_PER_SM)
+__global__ void __launch_bounds__(160, decode_ctas_per_sm(DK, DV, NQ))
 attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const DecodeParams p)
 {
-    using L = Layout<DK, DV>;
+    using L = Layout<DK, DV, decode_ctas_per_sm(DK, DV, NQ)>;
+    static_assert(L::NUM_THREADS == 160, "launch bounds");
     griddep_wait();   // the previous grid's writes (Q, the cache, the lengths) are visible
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -275,6 +280,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constan
     }
 
     // ---------------------------------------------- merge the four warps
+    // (the merge area may be the key stage: every warp must be done with the last tile)
+    if (L::RED_IN_STAGE) asm volatile("bar.sync 1, 128;" ::: "memory");
     float* red = sred + warp * (L::RED_WARP / 4);
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
@@ -349,7 +356,7 @@ attn_decode_combine_kernel(const DecodeParams p)
 template <int DK, int DV, int NQ>
 cudaError_t launch(const CUtensorMap& tmK, const CUtensorMap& tmV, const DecodeParams& p, cudaStream_t stream)
 {
-    using L = Layout<DK, DV>;
+    using L = Layout<DK, DV, decode_ctas_per_sm(DK, DV, NQ)>;
     auto kern = attn_decode_kernel<DK, DV, NQ>;
     static bool configured[64] = {};
     int dev = 0;
