@@ -179,6 +179,38 @@ def test_bwd_full_size_identities_and_sampled_heads():
             assert np.all(np.abs(G - R) <= 2 * bd + 1e-6), (name, b, h)
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128)])
+@pytest.mark.parametrize("mask,n,m,lens", [
+    ("causal", 300, 130, None),                     # rows 0..169 see no key
+    ("key_padding", 97, 200, [200, 0, 33]),         # an entry without keys; 97 = 3 * 32 + 1 rows
+    ("causal_cache", 70, 300, [300, 70, 150, 0]),   # the queries end each entry's filled cache
+])
+def test_bwd_every_output_written(dk, dv, mask, n, m, lens):
+    """Outputs pre-filled with NaN and a workspace of 0xFF bytes, used for two calls:
+    every element of dQ, dK and dV is written (rows that no key tile adds to, the
+    partial last 32-row group), whatever the workspace held on entry, and both calls
+    match the oracle."""
+    B, H = (len(lens) if lens else 2), 2
+    x = inputs.make_inputs(B, H, n, m, dk, dv, mask, seed=8700 + n + dk + dv, key_lengths=lens)
+    dO = inputs.make_grad_output(B, H, n, dv, seed=8701 + n)
+    Q, K, V, g = x.Q.cuda(), x.K.cuda(), x.V.cuda(), dO.cuda()
+    lens_d = x.key_lengths.cuda() if x.key_lengths is not None else None
+    O, LSE = attn.attn_fwd(Q, K, V, x.mask, lens_d, x.scale)
+    ws = torch.full((attn.bwd_workspace_size(B, H, n, m, dk, dv),), 255, dtype=torch.uint8, device="cuda")
+    refs = oracle.attn_bwd(x.Q, x.K, x.V, dO, x.mask, x.key_lengths, x.scale)
+    bds = bounds(x, dO, refs)
+    for call in range(2):
+        outs = [torch.full(shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+                for shape in ((B, H, n, dk), (B, H, m, dk), (B, H, m, dv))]
+        attn.attn_bwd(Q, K, V, O, LSE, g, x.mask, lens_d, x.scale, *outs, workspace=ws)
+        rc, detail = attn.device_status()
+        assert rc == attn.ATTN_OK, (rc, detail)
+        for name, G, R, bd in zip(("dQ", "dK", "dV"), outs, refs, bds):
+            G = G.float().cpu().numpy()
+            assert np.all(np.isfinite(G)), f"call {call}: {name} has unwritten elements"
+            assert np.all(np.abs(G - R) <= 2 * bd + 1e-6), f"call {call}: {name}"
+
+
 def test_bwd_dk_dv_deterministic():
     x, dO = case(2, 3, 300, 300, 64, "causal", seed=8500)
     a = run_gpu_bwd(x, dO)

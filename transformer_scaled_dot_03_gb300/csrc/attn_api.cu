@@ -450,47 +450,59 @@ BwdWorkspace bwd_workspace(int64_t bh, int64_t n, int64_t d_k)
 }
 
 // D_i = sum_c dO_ic O_ic (fp32 from the bf16 tensors) and LSE_i * log2(e) for every
-// row of the padded layout (0 in the padding); zeroes the dQ accumulator. A group of
-// d_v / 8 lanes reads one row, 16 bytes per lane.
+// row of the padded layout (0 in the padding), and the row's d_k accumulator
+// entries zeroed, in one pass over the rows, so that the reads of O and dO and the
+// zero writes stream together. A group of G = d_v / 8 lanes takes a row (16 bytes
+// of O and of dO per lane, d_k / (4 G) float4 of zeros); a warp takes two sets of
+// 32 / G rows per iteration, so that every lane has four 16-byte loads in flight.
 __global__ void bwd_prep_kernel(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
-                                const float* __restrict__ LSE, int64_t bh_count, int n, int64_t n_pad, int d_v,
-                                float* __restrict__ lse2, float* __restrict__ dd, float4* __restrict__ dq_acc,
-                                int64_t dq_vec)
+                                const float* __restrict__ LSE, int64_t bh_count, int n, int64_t n_pad, int d_k,
+                                int d_v, float* __restrict__ lse2, float* __restrict__ dd, float4* __restrict__ dq_acc)
 {
     sm103a::griddep_wait();   // O, dO and LSE of the earlier kernels are visible
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = tid; i < dq_vec; i += stride) dq_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-
     const int G = d_v / 8;                       // lanes per row: 8 or 16
     const int lane = threadIdx.x % 32;
     const int g = lane % G;
-    const int rows_per_warp = 32 / G;
+    const int zq = d_k / 4;                      // float4 per accumulator row
     const int64_t total = bh_count * n_pad;
-    const int64_t warp_id = tid / 32;
-    const int64_t warp_stride = stride / 32;
-    for (int64_t r0 = warp_id * rows_per_warp; r0 < total; r0 += warp_stride * rows_per_warp) {
-        const int64_t row = r0 + lane / G;
-        const int64_t bh = row / n_pad;
-        const int64_t q = row - bh * n_pad;
-        const bool valid = row < total && q < n;
-        float acc = 0.f;
-        if (valid) {
-            const int64_t e0 = (bh * n + q) * d_v + 8 * g;
-            const uint4 a = *reinterpret_cast<const uint4*>(O + e0);
-            const uint4 b = *reinterpret_cast<const uint4*>(dO + e0);
-            const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-            const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x / 32 * (32 / G);   // rows per sweep
+    for (int64_t base = warp_id * (32 / G); base < total; base += 2 * step) {
+        uint4 a[2], b[2];
+        float lz[2];
+        bool valid[2];
+        int64_t row[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            row[u] = base + u * step + lane / G;
+            const int64_t bh = row[u] / n_pad;
+            const int64_t q = row[u] - bh * n_pad;
+            valid[u] = row[u] < total && q < n;
+            a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+            lz[u] = 0.f;
+            if (valid[u]) {
+                const int64_t r = bh * n + q;
+                a[u] = *reinterpret_cast<const uint4*>(O + r * d_v + 8 * g);
+                b[u] = *reinterpret_cast<const uint4*>(dO + r * d_v + 8 * g);
+                if (g == 0) lz[u] = LSE[r];
+                for (int i = g; i < zq; i += G) dq_acc[r * zq + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+            const uint32_t bv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+            float acc = 0.f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 acc = fmaf(__uint_as_float(av[k] << 16), __uint_as_float(bv[k] << 16), acc);
                 acc = fmaf(__uint_as_float(av[k] & 0xFFFF0000u), __uint_as_float(bv[k] & 0xFFFF0000u), acc);
             }
-        }
-        for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (g == 0 && row < total) {
-            dd[row] = valid ? acc : 0.f;
-            lse2[row] = valid ? LSE[bh * n + q] * kLog2e : 0.f;
+            for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (g == 0 && row[u] < total) {
+                dd[row[u]] = valid[u] ? acc : 0.f;
+                lse2[row[u]] = valid[u] ? lz[u] * kLog2e : 0.f;
+            }
         }
     }
 }
@@ -611,10 +623,10 @@ int bwd_impl(const void* Q, const void* K, const void* V, const void* O, const v
     p.debug_flags = g_debug_flags;
 
     const int64_t dq_vec = bh * n * d_k / 4;
-    const int64_t prep_threads = std::max<int64_t>(dq_vec, bh * ws.n_pad * (d_v / 8));
+    const int64_t prep_threads = (bh * ws.n_pad * (d_v / 8) + 1) / 2;   // two rows per lane group
     cudaError_t e = attn::launch_pdl(bwd_prep_kernel, dim3(static_cast<unsigned>(grid_for(prep_threads, 256))), dim3(256),
                                      0, st, static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), LSE,
-                                     bh, n, ws.n_pad, d_v, lse2, dd, reinterpret_cast<float4*>(dq_acc), dq_vec);
+                                     bh, n, ws.n_pad, d_k, d_v, lse2, dd, reinterpret_cast<float4*>(dq_acc));
     if (e != cudaSuccess) return fail_cuda("backward preparation kernel launch", e);
     if (slopes != nullptr)
         e = attn::launch_bwd_alibi(d_k, d_v, mask_kind, maps, p, st);
