@@ -467,6 +467,7 @@ __global__ void bwd_prep_kernel(const uint16_t* __restrict__ O, const uint16_t* 
     const int64_t total = bh_count * n_pad;
     const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / 32;
     const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x / 32 * (32 / G);   // rows per sweep
+    const uint64_t keep = sm103a::l2_policy_evict_last();   // the accumulator is added into and read back next
     for (int64_t base = warp_id * (32 / G); base < total; base += 2 * step) {
         uint4 a[2], b[2];
         float lz[2];
@@ -485,7 +486,10 @@ __global__ void bwd_prep_kernel(const uint16_t* __restrict__ O, const uint16_t* 
                 a[u] = *reinterpret_cast<const uint4*>(O + r * d_v + 8 * g);
                 b[u] = *reinterpret_cast<const uint4*>(dO + r * d_v + 8 * g);
                 if (g == 0) lz[u] = LSE[r];
-                for (int i = g; i < zq; i += G) dq_acc[r * zq + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int i = g; i < zq; i += G)
+                    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %1, %1, %1}, %2;" ::"l"(dq_acc + r * zq + i),
+                                 "f"(0.f), "l"(keep)
+                                 : "memory");
             }
         }
 #pragma unroll

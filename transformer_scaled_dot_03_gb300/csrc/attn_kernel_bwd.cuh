@@ -51,6 +51,20 @@ constexpr int BM = 128;   // query rows per tile
 constexpr int BN = 128;   // keys per CTA
 constexpr int CHUNK_BYTES = 128 * 64 * 2;
 
+// The dQ reduce-add (3-D tiled, shared -> global, bulk group) with an L2 evict_last
+// policy: the fp32 accumulator is zeroed, added into and read back within one
+// backward pass, and the streamed Q, K, V and dO tiles should leave L2 before it
+// does (the preparation kernel's zero stores carry the same policy).
+__device__ __forceinline__ void dq_reduce_add(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1,
+                                              int32_t c2)
+{
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(l2_policy_evict_last())
+        : "memory");
+}
+
 // DK: query/key head dim, DV: value head dim.
 template <int DK, int DV>
 struct Layout {
@@ -447,7 +461,7 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && q0 + 32 * wq < p.n) {
-                    tma_reduce_add_3d(&maps.dq_acc, sdS + half * CHUNK_BYTES + wq * 32 * 128, col, q0 + 32 * wq, bh);
+                    dq_reduce_add(&maps.dq_acc, sdS + half * CHUNK_BYTES + wq * 32 * 128, col, q0 + 32 * wq, bh);
                     bulk_commit_group();
                     store_pending = true;
                 }
@@ -533,6 +547,8 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 // so the tensor cores compute the next tile's scores while the softmax warps turn
 // tile t's into Pᵀ and dS (warp 10 issues the scores, warp 9 the products). The dQ
 // of a tile is read out one iteration later, through a staging area of its own.
+// Warp 11 is idle: it completes the control warpgroup (8-11), whose registers go to
+// the compute warps by setmaxnreg.
 //
 // Persistent: one CTA per SM walks work items (b, h, 128-key tile) round-robin;
 // under the causal masks a unit pairs key tile k with key tile nkb-1-k of the same
@@ -546,11 +562,17 @@ attn_bwd_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
 struct LayoutPipe {
     static constexpr int D = 64;
     static constexpr int TILE = CHUNK_BYTES;                 // a 128 x 64 bf16 tile
-    static constexpr int NUM_THREADS = 352;
+    static constexpr int NUM_THREADS = 384;                  // warp 11 idle: completes the control warpgroup
     static constexpr int COMPUTE_THREADS = 256;
     static constexpr int WARP_TMA = 8;
     static constexpr int WARP_MMA = 9;                       // issues the products, owns the tensor memory
     static constexpr int WARP_MMA_S = 10;                    // issues the scores
+    // registers per thread: the launch's share, then re-balanced by setmaxnreg from
+    // the control warpgroup (warps 8-11) to the two compute warpgroups
+    static constexpr uint32_t REG_LAUNCH = 65536 / NUM_THREADS / 8 * 8;
+    static constexpr uint32_t REG_CTRL = 72;
+    static constexpr uint32_t REG_COMPUTE = (REG_LAUNCH * NUM_THREADS - REG_CTRL * 128) / 256 / 8 * 8;
+    static_assert(256 * REG_COMPUTE + 128 * REG_CTRL <= REG_LAUNCH * NUM_THREADS, "register split");
     static constexpr int QS = 2;                             // Q/dO/LSE/D ring depth
     static constexpr int KVS = 2;                            // K/V buffers
     static constexpr int K_OFF = 0;
@@ -733,6 +755,7 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
     const uint32_t sdQ = sbase + L::DQ_OFF;
 
     if (warp >= L::WARP_TMA) {
+        regs_dec<L::REG_CTRL>();
         if (warp == L::WARP_TMA && lane == 0) {
             // ================================================== TMA producer
             BwdCursor<MASK> cur;
@@ -900,6 +923,7 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
         __syncwarp();
     } else {
         // ================================================== Pᵀ / dS, dQ read-out, epilogue
+        regs_inc<L::REG_COMPUTE>();
         const int wq = warp % 4;                      // lane quadrant
         const int half = warp / 4;                    // column half
         const int r = 32 * wq + lane;                 // TMEM lane: a key here, a query row for dQ
@@ -939,8 +963,8 @@ attn_bwd_pipe_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && prev_q0 + 32 * wq < p.n) {
-                tma_reduce_add_3d(&maps.dq_acc, sdQ + half * CHUNK_BYTES + wq * 32 * 128, 32 * half,
-                                  prev_q0 + 32 * wq, prev_bh);
+                dq_reduce_add(&maps.dq_acc, sdQ + half * CHUNK_BYTES + wq * 32 * 128, 32 * half, prev_q0 + 32 * wq,
+                              prev_bh);
                 bulk_commit_group();
                 bulk_pending = true;
             }

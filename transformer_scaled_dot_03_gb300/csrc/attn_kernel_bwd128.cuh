@@ -458,8 +458,8 @@ attn_bwd_pipe128_kernel(const __grid_constant__ BwdMaps maps, const BwdParams p)
                     if (lane == 0) {
                         for (int h = 0; h < 2; ++h) {
                             if (q0 + 32 * h >= p.n) break;
-                            tma_reduce_add_3d(&maps.dq_acc, sdQ + static_cast<uint32_t>(h * 4 + wq) * DQ_BLOCK, 32 * wq,
-                                              q0 + 32 * h, w.bh);
+                            bwd::dq_reduce_add(&maps.dq_acc, sdQ + static_cast<uint32_t>(h * 4 + wq) * DQ_BLOCK, 32 * wq,
+                                               q0 + 32 * h, w.bh);
                         }
                         bulk_commit_group();
                         bulk_pending = true;
