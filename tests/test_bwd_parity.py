@@ -149,11 +149,12 @@ def test_bwd_sharp_rows():
     check_bwd(x, dO, "sharp")
 
 
-def test_bwd_full_size_identities_and_sampled_heads():
-    """Big-decoder workload at full size (16 x 16 heads) under the decoder target mask:
-    the softmax identities hold on the GPU's gradients for every head (dK sums to zero
-    over the keys of a head; dV sums to the dO of the rows that see a key), and a
-    seeded set of 16 (b, h) pairs matches the oracle element by element."""
+def test_bwd_full_size_every_head():
+    """Big-decoder workload at full size (16 x 16 heads, n = m = 1024) under the
+    decoder target mask, in one launch: the softmax identities hold on the GPU's
+    gradients for every head (dK sums to zero over the keys of a head; dV sums to the
+    dO of the rows that see a key), and every element of dQ, dK and dV of every head
+    matches the oracle within the bound (the oracle runs four heads at a time)."""
     B, H, n, d = 16, 16, 1024, 64
     x = inputs.make_inputs(B, H, n, n, d, d, "causal_key_padding", seed=8400, len_lo=512, len_hi=n)
     dO = inputs.make_grad_output(B, H, n, d, seed=8401)
@@ -166,17 +167,16 @@ def test_bwd_full_size_identities_and_sampled_heads():
     assert np.all(np.abs(dK.sum(axis=2)) <= 2.0 ** -6 * scale_k + 1e-3)
     dv_sum = dV.sum(axis=2)
     np.testing.assert_allclose(dv_sum, g.sum(axis=2), atol=2.0 ** -6 * np.abs(g).sum(axis=2).max())
-    gen = torch.Generator().manual_seed(8402)
-    pairs = torch.randperm(B * H, generator=gen)[:14].tolist() + [0, B * H - 1]
-    for bh in sorted(set(pairs)):
-        b, h = divmod(bh, H)
-        xs = inputs.Inputs(x.Q[b:b + 1, h:h + 1].contiguous(), x.K[b:b + 1, h:h + 1].contiguous(),
-                           x.V[b:b + 1, h:h + 1].contiguous(), x.key_lengths[b:b + 1].clone(), x.mask, x.scale)
-        gs = dO[b:b + 1, h:h + 1].contiguous()
-        refs = oracle.attn_bwd(xs.Q, xs.K, xs.V, gs, xs.mask, xs.key_lengths, xs.scale)
-        for name, G, R, bd in zip(("dQ", "dK", "dV"), (dQ[b:b + 1, h:h + 1], dK[b:b + 1, h:h + 1],
-                                                       dV[b:b + 1, h:h + 1]), refs, bounds(xs, gs, refs)):
-            assert np.all(np.abs(G - R) <= 2 * bd + 1e-6), (name, b, h)
+    for b in range(B):
+        for h0 in range(0, H, 4):
+            hs = slice(h0, h0 + 4)
+            xs = inputs.Inputs(x.Q[b:b + 1, hs].contiguous(), x.K[b:b + 1, hs].contiguous(),
+                               x.V[b:b + 1, hs].contiguous(), x.key_lengths[b:b + 1].clone(), x.mask, x.scale)
+            gs = dO[b:b + 1, hs].contiguous()
+            refs = oracle.attn_bwd(xs.Q, xs.K, xs.V, gs, xs.mask, xs.key_lengths, xs.scale)
+            for name, G, R, bd in zip(("dQ", "dK", "dV"), (dQ[b:b + 1, hs], dK[b:b + 1, hs], dV[b:b + 1, hs]),
+                                      refs, bounds(xs, gs, refs)):
+                assert np.all(np.abs(G - R) <= 2 * bd + 1e-6), (name, b, h0)
 
 
 @pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128)])
