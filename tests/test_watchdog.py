@@ -48,14 +48,15 @@ def test_forced_timeout_reports_and_recovers(mask, d):
     assert np.abs(L.cpu().numpy() - Lr).max() <= 1e-3
 
 
-@pytest.mark.parametrize("d", [64, 128])
-def test_forced_timeout_in_the_backward(d):
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 128), (64, 128)])
+def test_forced_timeout_in_the_backward(dk, dv):
     """The same for the backward kernels (the persistent 128-query-tile kernel at
     d = 64, the 64-query-step kernel with two MMA issuers and a read-out warpgroup at
-    d = 128): the forced wait gives up, the status reports it, every role leaves, and a
-    normal backward afterwards matches the oracle."""
-    x = inputs.make_inputs(2, 2, 260, 260, d, d, "causal", seed=5100 + d)
-    dO = inputs.make_grad_output(2, 2, 260, d, seed=5101 + d)
+    d = 128, the one-tile-per-CTA kernel for d_k != d_v): the forced wait gives up,
+    the status reports it, every role leaves, and a normal backward afterwards
+    matches the oracle."""
+    x = inputs.make_inputs(2, 2, 260, 260, dk, dv, "causal", seed=5100 + dk + dv)
+    dO = inputs.make_grad_output(2, 2, 260, dv, seed=5101 + dk + dv)
     Q, K, V, g = x.Q.cuda(), x.K.cuda(), x.V.cuda(), dO.cuda()
     O, L = attn.attn_fwd(Q, K, V, x.mask, None, x.scale)
     assert attn.device_status() == (attn.ATTN_OK, 0)
